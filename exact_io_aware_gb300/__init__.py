@@ -1,0 +1,182 @@
+"""exact_io_aware_gb300 — exact tiled softmax attention on GB300, Python binding.
+
+A thin ctypes layer over the C ABI in ``include/exactattn.h`` (``lib/libexactattn.so``):
+it checks tensor shapes, allocates outputs with PyTorch and passes raw device pointers and
+the current CUDA stream.  All arithmetic runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback, and every entry point raises if the library is not built.
+
+    o, lse = attn_fwd(q, k, v, c, mask="causal")
+    dq, dk, dv = attn_bwd(q, k, v, o, lse, do, c, mask="causal")
+    y = attention(q, k, v, c, mask="causal")      # autograd-aware wrapper
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+    "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
+    "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
+    "attn_device_status", "attn_last_error", "attention",
+]
+
+ATTN_OK = 0
+ATTN_WARN_EMPTY_ROW = 1
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_ALIGNMENT = -3
+ATTN_ERR_WORKSPACE = -4
+ATTN_ERR_CUDA = -5
+ATTN_ERR_DEVICE_TIMEOUT = -6
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+MASK_CODE = {"none": 0, "causal": 1, "bitmap": 2}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"exactattn error {code}: {message}")
+        self.code = code
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libexactattn.so")
+
+
+def load():
+    """Load the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with exact_io_aware_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64, i32,
+                             vp, vp, vp]
+    lib.attn_fwd.restype = i32
+    lib.attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.attn_bwd_workspace_bytes.restype = sz
+    lib.attn_bwd.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, i32, vp, i64,
+                             i64, i32, vp, vp, vp, vp, sz, vp]
+    lib.attn_bwd.restype = i32
+    lib.attn_device_status.argtypes = [vp]
+    lib.attn_device_status.restype = i32
+    lib.attn_last_error.argtypes = []
+    lib.attn_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def attn_last_error() -> str:
+    return load().attn_last_error().decode()
+
+
+def _check(rc: int):
+    if rc < 0:
+        raise AttnError(rc, attn_last_error())
+    return rc
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _shape(q, k, v):
+    if q.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, n, d]")
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k and v must have the same shape (n_q = n_k, v = d)")
+    if q.dtype not in DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype among float32, float16, bfloat16")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    return q.shape
+
+
+def _mask_args(mask, mask_bits, mask_head_stride_words):
+    kind = MASK_CODE[mask]
+    if kind != 2:
+        return kind, None, 0, 0
+    if mask_bits is None or not mask_bits.is_cuda or not mask_bits.is_contiguous():
+        raise ValueError("bitmap mask needs a contiguous CUDA int32 tensor [..., n, row_words]")
+    if mask_bits.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("mask_bits must hold 32-bit words")
+    return kind, mask_bits, int(mask_bits.shape[-1]), int(mask_head_stride_words)
+
+
+def attn_fwd(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=0, kv_block=0,
+             o=None, lse=None, stream=None):
+    """Forward pass; returns (o [B,H,n,d], lse [B,H,n] float32)."""
+    B, H, n, d = _shape(q, k, v)
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
+    _check(load().attn_fwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
+                           kind, _ptr(bits), row_words, hs, int(kv_block), _ptr(o), _ptr(lse),
+                           _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_bwd_workspace_bytes(dtype, B, H, n, d) -> int:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().attn_bwd_workspace_bytes(code, B, H, n, d))
+
+
+def attn_bwd(q, k, v, o, lse, do, c, mask="none", mask_bits=None, mask_head_stride_words=0,
+             kv_block=0, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass (vector-Jacobian product for upstream ``do``); returns (dq, dk, dv)."""
+    B, H, n, d = _shape(q, k, v)
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = attn_bwd_workspace_bytes(q.dtype, B, H, n, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(load().attn_bwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
+                           _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits), row_words, hs,
+                           int(kv_block), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return dq, dk, dv
+
+
+def attn_device_status(stream=None) -> int:
+    """Synchronise the stream; return and clear the device status word (see the header)."""
+    return _check(load().attn_device_status(_stream_ptr(stream)))
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, c, mask, mask_bits, kv_block):
+        o, lse = attn_fwd(q, k, v, c, mask, mask_bits, 0, kv_block)
+        ctx.save_for_backward(q, k, v, o, lse, mask_bits)
+        ctx.c, ctx.mask, ctx.kv_block = c, mask, kv_block
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse, mask_bits = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), ctx.c, ctx.mask, mask_bits, 0,
+                              ctx.kv_block)
+        return dq, dk, dv, None, None, None, None
+
+
+def attention(q, k, v, c, mask="none", mask_bits=None, kv_block=0):
+    """Differentiable exact attention O = softmax(c QKᵀ + mask) V."""
+    return _Attention.apply(q, k, v, c, mask, mask_bits, kv_block)

@@ -1,0 +1,184 @@
+// C ABI of the exact tiled attention library: argument checks, dispatch to the kernels,
+// error reporting and the device status word.  See include/exactattn.h for the contract.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <string>
+
+#include "exactattn.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+// One status word per device, in static device memory (no allocation).  Kernels OR flags
+// into it; attn_device_status reads and clears it.
+__device__ uint32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int status_ptr(uint32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal too large");
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess)
+      return fail(ATTN_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int dtype, int B, int H, int n, int d, const void* q, const void* k,
+                 const void* v, int mask_kind, const uint32_t* bits, int64_t row_words,
+                 int64_t head_stride, int kv_block) {
+  if (dtype < ATTN_F32 || dtype > ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype");
+  if (B < 1 || H < 1 || n < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and n must be positive");
+  if (d != 16 && d != 32 && d != 64 && d != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head dimension must be 16, 32, 64 or 128");
+  if (static_cast<int64_t>(B) * H > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "B * H must be at most 65535");
+  if (kv_block != 0 && kv_block != 32 && kv_block != 64 && kv_block != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "kv_block must be 0, 32, 64 or 128");
+  if (!q || !k || !v) return fail(ATTN_ERR_INVALID_ARG, "null input pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v))
+    return fail(ATTN_ERR_ALIGNMENT, "q, k and v must be 16-byte aligned");
+  if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_BITMAP)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind");
+  if (mask_kind == ATTN_MASK_BITMAP) {
+    if (!bits) return fail(ATTN_ERR_INVALID_ARG, "bitmap mask without mask_bits");
+    if ((reinterpret_cast<uintptr_t>(bits) & 3u) != 0)
+      return fail(ATTN_ERR_ALIGNMENT, "mask_bits must be 4-byte aligned");
+    if (row_words < (n + 31) / 32) return fail(ATTN_ERR_INVALID_ARG, "mask_row_words < ceil(n/32)");
+    if (head_stride < 0) return fail(ATTN_ERR_INVALID_ARG, "negative mask_head_stride_words");
+  }
+  return ATTN_OK;
+}
+
+ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const void* k,
+                       const void* v, int mask_kind, const uint32_t* bits, int64_t row_words,
+                       int64_t head_stride, int kv_block) {
+  ea::AttnArgs a{};
+  a.B = B;
+  a.H = H;
+  a.n = n;
+  a.d = d;
+  a.c = c;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.mask_kind = mask_kind;
+  a.mask_bits = mask_kind == ATTN_MASK_BITMAP ? bits : nullptr;
+  a.mask_row_words = row_words;
+  a.mask_head_stride_words = head_stride;
+  a.kv_block = kv_block;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+             const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+             int64_t mask_head_stride_words, int kv_block, void* o, float* lse, void* stream) {
+  if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
+                            mask_head_stride_words, kv_block))
+    return rc;
+  if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
+  if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  ea::AttnArgs a = make_args(B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                             mask_head_stride_words, kv_block);
+  a.o_out = o;
+  a.lse = lse;
+  if (int rc = status_ptr(&a.status)) return rc;
+  std::string err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = dtype == ATTN_F32 ? ea::launch_fwd_f32(a, s, err)
+                             : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int n, int d) {
+  if (B < 1 || H < 1 || n < 1 || d < 1) return 0;
+  return dtype == ATTN_F32 ? ea::bwd_f32_workspace_bytes(B, H, n, d)
+                           : ea::bwd_tc_workspace_bytes(B, H, n, d);
+}
+
+int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+             const void* v, const void* o, const float* lse, const void* d_o, int mask_kind,
+             const uint32_t* mask_bits, int64_t mask_row_words, int64_t mask_head_stride_words,
+             int kv_block, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+             void* stream) {
+  if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
+                            mask_head_stride_words, kv_block))
+    return rc;
+  if (!o || !lse || !d_o) return fail(ATTN_ERR_INVALID_ARG, "null o, lse or d_o");
+  if (!dq || !dk || !dv) return fail(ATTN_ERR_INVALID_ARG, "null gradient pointer");
+  if (!aligned16(o) || !aligned16(d_o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return fail(ATTN_ERR_ALIGNMENT, "o, d_o, dq, dk and dv must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  const size_t need = attn_bwd_workspace_bytes(dtype, B, H, n, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace missing or smaller than attn_bwd_workspace_bytes");
+  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  ea::AttnArgs a = make_args(B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                             mask_head_stride_words, kv_block);
+  a.o = o;
+  a.lse = const_cast<float*>(lse);
+  a.d_o = d_o;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  if (int rc = status_ptr(&a.status)) return rc;
+  std::string err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = dtype == ATTN_F32 ? ea::launch_bwd_f32(a, s, err)
+                             : ea::launch_bwd_tc(dtype == ATTN_BF16, a, s, err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
+int attn_device_status(void* stream) {
+  uint32_t* p = nullptr;
+  if (int rc = status_ptr(&p)) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(word));
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, std::string("status word: ") + cudaGetErrorString(e));
+  if (word & 1u) {
+    char buf[96];
+    snprintf(buf, sizeof(buf), "an in-kernel wait gave up (sites 0x%02x)", (word >> 8) & 0xFFu);
+    return fail(ATTN_ERR_DEVICE_TIMEOUT, buf);
+  }
+  if (word & 2u) return ATTN_WARN_EMPTY_ROW;
+  return ATTN_OK;
+}
+
+const char* attn_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,460 @@
+// Forward pass of exact tiled softmax attention on the tcgen05 tensor cores (fp16 / bf16).
+//
+// Follows the tiled forward procedure of "Exact tiled attention and memory-aware
+// differentiation": key blocks J_t are visited in order, blocks with no allowed key are
+// skipped, each query row keeps the summary (m, l, z) and merges every new block into it,
+// and at the end O_i = z_i / l_i.  Retained statistic: LSE_i = m_i + ln l_i.
+//
+// One CTA owns two tiles of 128 query rows of one head (256 rows).  Roles:
+//   warps 0-3  softmax for tile 0   (thread = query row = TMEM lane)
+//   warps 4-7  softmax for tile 1
+//   warp  8    TMA producer: Q tiles once, then K and V blocks through an NS-stage ring
+//   warp  9    TMEM allocator and MMA issuer (one elected thread)
+// Tensor memory: S_t = Q_t K_jᵀ (BN fp32 columns per tile; the 16-bit P_t is written over
+// the first BN/2 of them) and O_t, the unnormalised weighted value sum z (D columns per tile).
+// The MMA thread issues, per key block, PV_{j-1}(t0), S_j(t0), PV_{j-1}(t1), S_j(t1), so the
+// tensor core works on one tile while the other tile's softmax runs.
+//
+// Online softmax (the running-maximum recurrence of "The Arithmetic of Intelligence",
+// chapter 12): scores are taken to base 2 with the folded factor c·log2(e) (the exp2
+// prescale described in "Bellek Duvarının Fiziği", online softmax section).  The running
+// maximum m is raised only when a block's maximum exceeds it by more than kLazy (2^8), and
+// then l and z are multiplied by e^{m-m'}; otherwise the stale m is kept and probabilities
+// up to 2^8 enter P.  The final z / l and m + log2 l are unchanged by this (a common shift of
+// every score cancels in z / l), and 2^8 stays far inside the fp16 range.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "tile.cuh"
+
+namespace ea {
+namespace fwd {
+
+constexpr int kRowsPerTile = 128;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLazy = 8.0f;  // log2 units
+constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
+
+template <int D, int BN>
+struct Config {
+  using TQ = Tile<kRowsPerTile, D>;
+  using TKV = Tile<BN, D>;
+  static constexpr int kSmemBudget = 227 * 1024 - 1024 - 512;  // minus alignment slack, barriers
+  static constexpr int kStageBytes = 2 * TKV::kBytes;          // one K block + one V block
+  static constexpr int kFixed = 2 * TQ::kBytes;
+  static constexpr int kMaxStepBytes = 16 * 1024;
+  static constexpr int kStagesFit = (kSmemBudget - kFixed - kMaxStepBytes) / kStageBytes;
+  static constexpr int NS = kStagesFit > 4 ? 4 : kStagesFit;
+  static_assert(NS >= 2, "need at least two pipeline stages");
+  static constexpr int kTmemCols = 2 * BN + 2 * D;
+  static constexpr int kTmemAlloc = kTmemCols <= 32    ? 32
+                                    : kTmemCols <= 64  ? 64
+                                    : kTmemCols <= 128 ? 128
+                                    : kTmemCols <= 256 ? 256
+                                                       : 512;
+  static_assert(kTmemCols <= 512, "tensor memory overflow");
+  // dynamic shared memory layout (offsets from a 1024-aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * TQ::kBytes;
+  static constexpr int kOffV = kOffK + NS * TKV::kBytes;
+  static constexpr int kOffSteps = kOffV + NS * TKV::kBytes;
+  static size_t smem_bytes(int n) {
+    const int nblk = (n + BN - 1) / BN;
+    return 1024 + kOffSteps + 4 * static_cast<size_t>(nblk) + 512;
+  }
+};
+
+struct Barriers {
+  uint64_t q_full[2];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done[2];
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint32_t tmem_base;
+  uint32_t nsteps;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <bool kBf16, int D, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  FwdParams p) {
+  using C = Config<D, BN>;
+  using TQ = typename C::TQ;
+  using TKV = typename C::TKV;
+  constexpr int NS = C::NS;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint32_t* steps = reinterpret_cast<uint32_t*>(smem + C::kOffSteps);
+  __shared__ Barriers bars;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int n = p.n;
+  const int bh = blockIdx.y;
+  const int pair = (gridDim.x - 1 - blockIdx.x);  // heaviest (causal) query tiles first
+  const int pair_row0 = pair * 2 * kRowsPerTile;  // tile t starts at pair_row0 + 128 t
+  const int nblk = (n + BN - 1) / BN;
+
+  // ---------------------------------------------------------------- prologue
+  if (tid == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.q_full[t], 1);
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], 4);
+      mbar_init(&bars.o_done[t], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
+
+  // Classify every key block for both tiles: skip / full / partial (mask needed).
+  for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
+  __syncthreads();
+  const bool tail = (n % BN) != 0;
+  if (p.mask_kind == kMaskBitmap) {
+    if (tid < kSoftmaxThreads) {
+      const int t = tid / kRowsPerTile;
+      const int row = pair_row0 + t * kRowsPerTile + (tid % kRowsPerTile);
+      const bool valid = row < n;
+      const uint32_t* rowbits =
+          p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
+          static_cast<int64_t>(valid ? row : 0) * p.mask_row_words;
+      for (int j = 0; j < nblk; ++j) {
+        bool any = false, all = true;
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < BN / 32; ++q) {
+            const int key0 = j * BN + q * 32;
+            if (key0 < n) {
+              uint32_t w = __ldg(rowbits + key0 / 32);
+              const int nk = n - key0;
+              const uint32_t live = nk >= 32 ? 0xFFFFFFFFu : ((1u << nk) - 1u);
+              w &= live;
+              any |= w != 0;
+              all &= w == live;
+            }
+          }
+        }
+        const bool wany = __any_sync(0xFFFFFFFFu, any);
+        const bool wall = __all_sync(0xFFFFFFFFu, all);
+        if (lane == 0) {
+          uint32_t bits = (wany ? (1u << t) : 0u) | (wall ? 0u : (4u << t));
+          if (bits) atomicOr(&steps[j], bits);
+        }
+      }
+    }
+  } else {
+    for (int j = tid; j < nblk; j += kThreads) {
+      uint32_t bits = 0;
+      for (int t = 0; t < 2; ++t) {
+        const int r0 = pair_row0 + t * kRowsPerTile;
+        const int last_row = min(r0 + kRowsPerTile, n) - 1;
+        if (r0 >= n) continue;
+        bool any = true, all = true;
+        if (p.mask_kind == kMaskCausal) {
+          any = j * BN <= last_row;
+          all = (j + 1) * BN - 1 <= r0;
+        }
+        if (any) bits |= (1u << t) | (all ? 0u : (4u << t));
+      }
+      steps[j] = bits;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int ns = 0;
+    for (int j = 0; j < nblk; ++j) {
+      const uint32_t b = steps[j];
+      const bool part_tail = tail && j == nblk - 1;
+      uint32_t cls0 = (b & 1u) ? (((b & 4u) || part_tail) ? kPartial : kFull) : kSkip;
+      uint32_t cls1 = (b & 2u) ? (((b & 8u) || part_tail) ? kPartial : kFull) : kSkip;
+      if (cls0 | cls1) steps[ns++] = static_cast<uint32_t>(j) | (cls0 << 16) | (cls1 << 18);
+    }
+    bars.nsteps = ns;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int nsteps = bars.nsteps;
+  const uint32_t tmem = bars.tmem_base;
+  // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*D
+  uint32_t act = 0;  // bit t: tile t takes part in some step
+  for (int i = 0; i < nsteps; ++i) act |= ((steps[i] >> 16) & 3u ? 1u : 0u) | ((steps[i] >> 18) & 3u ? 2u : 0u);
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!((act >> t) & 1u)) continue;
+        mbar_arrive_expect_tx(&bars.q_full[t], TQ::kBytes);
+#pragma unroll
+        for (int b = 0; b < TQ::L::kBoxes; ++b)
+          tma_load_3d(sQ + t * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.q_full[t],
+                      b * TQ::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
+      }
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % NS;
+        const uint32_t ph = (i / NS) & 1;
+        const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
+        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, p.status, 1)) break;
+        mbar_arrive_expect_tx(&bars.k_full[s], TKV::kBytes);
+#pragma unroll
+        for (int b = 0; b < TKV::L::kBoxes; ++b)
+          tma_load_3d(sK + s * TKV::kBytes + b * TKV::kBoxBytes, &tm_k, &bars.k_full[s],
+                      b * TKV::L::kBoxCols, key0, bh);
+        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, p.status, 2)) break;
+        mbar_arrive_expect_tx(&bars.v_full[s], TKV::kBytes);
+#pragma unroll
+        for (int b = 0; b < TKV::L::kBoxes; ++b)
+          tma_load_3d(sV + s * TKV::kBytes + b * TKV::kBoxBytes, &tm_v, &bars.v_full[s],
+                      b * TKV::L::kBoxCols, key0, bh);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    // Per step i: wait K_i; for each tile, first the PV of its previous step (if it took
+    // part), then S_i if it takes part.  Every PV is issued in the step right after its S, so
+    // each V stage is released one step after it was filled.
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);
+      constexpr uint32_t id_o = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);
+      bool ok = true;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (ok && ((act >> t) & 1u)) ok = mbar_wait(&bars.q_full[t], 0, p.status, 3);
+      uint32_t pend = 0;     // bit t: tile t took part in the previous step (PV owed)
+      uint32_t started = 0;  // bit t: O_t already holds a partial sum
+      uint32_t pph = 0;      // bit t: parity of the next p_full[t] phase
+      for (int i = 0; i <= nsteps && ok; ++i) {
+        const int prev = i - 1;
+        if (pend) {
+          ok = mbar_wait(&bars.v_full[prev % NS], (prev / NS) & 1, p.status, 5);
+          if (!ok) break;
+        }
+        const uint32_t cur = i < nsteps ? steps[i] : 0u;
+        const int s = i % NS;
+        if (i < nsteps) {
+          ok = mbar_wait(&bars.k_full[s], (i / NS) & 1, p.status, 6);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sK + s * TKV::kBytes);
+        const uint32_t vbase = smem_u32(sV + (prev >= 0 ? prev % NS : 0) * TKV::kBytes);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (ok && ((pend >> t) & 1u)) {
+            ok = mbar_wait(&bars.p_full[t], (pph >> t) & 1u, p.status, 4);
+            if (ok) {
+              pph ^= 1u << t;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk)
+                mma_ts(tmem + 2 * BN + t * D, tmem + t * BN + kk * 8, TKV::desc_mn(vbase, kk),
+                       id_o, (((started >> t) & 1u) || kk > 0) ? 1u : 0u);
+              started |= 1u << t;
+            }
+          }
+          if (ok && ((cur >> (16 + 2 * t)) & 3u)) {
+            const uint32_t qbase = smem_u32(sQ + t * TQ::kBytes);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(tmem + t * BN, TQ::desc_k(qbase, kk), TKV::desc_k(kbase, kk), id_s,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(&bars.s_full[t]);
+          }
+        }
+        if (!ok) break;
+        if (i < nsteps) mma_commit(&bars.k_empty[s]);
+        if (pend) mma_commit(&bars.v_empty[prev % NS]);
+        pend = (((cur >> 16) & 3u) ? 1u : 0u) | (((cur >> 18) & 3u) ? 2u : 0u);
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if ((act >> t) & 1u) mma_commit(&bars.o_done[t]);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax (tile t)
+    const int t = warp / 4;
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;
+    const int row = pair_row0 + t * kRowsPerTile + r;
+    const uint32_t tS = tmem + t * BN;
+    const uint32_t tO = tmem + 2 * BN + t * D;
+    const bool active = (act >> t) & 1u;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.c * 1.4426950408889634f;
+    float m = -INFINITY;  // running maximum, log2 units (possibly stale by < kLazy)
+    float l = 0.0f;       // running normaliser relative to m
+    uint32_t s_phase = 0;
+    bool first = true;
+    bool ok = active;
+    const uint32_t* rowbits =
+        p.mask_kind == kMaskBitmap
+            ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
+                  static_cast<int64_t>(row < n ? row : 0) * p.mask_row_words
+            : nullptr;
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const uint32_t cls = (steps[i] >> (16 + 2 * t)) & 3u;
+      if (cls == kSkip) continue;
+      const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
+      ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
+      if (!ok) break;
+      s_phase ^= 1;
+      tc_fence_after();
+      float sv[BN];
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS + lane_off + c0, rr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) sv[c0 + k] = __uint_as_float(rr[k]) * sl2;
+      }
+      if (cls == kPartial) {
+        if (p.mask_kind == kMaskCausal) {
+#pragma unroll
+          for (int k = 0; k < BN; ++k)
+            if (key0 + k > row || key0 + k >= n) sv[k] = -INFINITY;
+        } else if (p.mask_kind == kMaskBitmap) {
+#pragma unroll
+          for (int q = 0; q < BN / 32; ++q) {
+            const int kq = key0 + q * 32;
+            uint32_t w = (row < n && kq < n) ? __ldg(rowbits + kq / 32) : 0u;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (!((w >> k) & 1u) || kq + k >= n) sv[q * 32 + k] = -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < BN; ++k)
+            if (key0 + k >= n) sv[k] = -INFINITY;
+        }
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int k = 1; k < BN; ++k) mx = fmaxf(mx, sv[k]);
+      float alpha = 1.0f;
+      if (mx > m + kLazy || (m == -INFINITY && mx != -INFINITY)) {
+        alpha = ex2(m - mx);  // m = -inf gives 0
+        m = mx;
+        l *= alpha;
+      }
+      const float mu = (m == -INFINITY) ? 0.0f : m;
+      // z *= alpha: only after the first block, and only if some row of this warp needs it.
+      if (!first && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t rr[16];
+          tmem_ld16(tO + lane_off + c0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) rr[k] = __float_as_uint(__uint_as_float(rr[k]) * alpha);
+          tmem_st16(tO + lane_off + c0, rr);
+        }
+      }
+      first = false;
+      float rowsum = 0.0f;
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float p0 = ex2(sv[c0 + 2 * k] - mu);
+          const float p1 = ex2(sv[c0 + 2 * k + 1] - mu);
+          rowsum += p0 + p1;
+          pk[k] = pack2<kBf16>(p0, p1);
+        }
+        tmem_st16(tS + lane_off + c0 / 2, pk);
+      }
+      l += rowsum;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full[t]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    // A tile with rows but no allowed key at all (possible only under a bitmap) writes zeros
+    // and -inf, like any other row with an empty allowed set.
+    if (pair_row0 + t * kRowsPerTile < n) {
+      if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      uint8_t* stage = sQ + t * TQ::kBytes;  // Q_t is dead once every MMA of tile t is done
+      if (ok) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t rr[16];
+          if (active) {
+            tmem_ld16(tO + lane_off + c0, rr);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) rr[k] = 0u;
+          }
+          uint32_t pk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pk[k] = pack2<kBf16>(__uint_as_float(rr[2 * k]) * inv,
+                                 __uint_as_float(rr[2 * k + 1]) * inv);
+          *reinterpret_cast<uint4*>(stage + TQ::offset(r, c0)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(stage + TQ::offset(r, c0 + 8)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        if (row < n) {
+          p.lse[static_cast<int64_t>(bh) * n + row] =
+              l > 0.0f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+          if (!(l > 0.0f)) raise_empty_row(p.status);
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier(1 + t, 128);
+      if (ok && r == 0) {
+#pragma unroll
+        for (int b = 0; b < TQ::L::kBoxes; ++b)
+          tma_store_3d(&tm_o, stage + b * TQ::kBoxBytes, b * TQ::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemAlloc);
+  }
+}
+
+}  // namespace fwd
+}  // namespace ea

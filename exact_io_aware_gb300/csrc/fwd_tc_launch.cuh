@@ -1,0 +1,65 @@
+// Host launcher for the tcgen05 forward kernel, instantiated per head dimension in
+// fwd_tc_d*.cu so the translation units compile in parallel.
+#pragma once
+#include <cstdio>
+
+#include "fwd_tc.cuh"
+#include "tmap.h"
+
+namespace ea {
+namespace fwd {
+
+// Opt-in shared memory per CTA on sm_103a is 227 KiB, of which the kernel's static barrier
+// block takes a few hundred bytes.
+constexpr int kMaxDynSmem = 227 * 1024 - 1024;
+
+template <bool kBf16, int D, int BN>
+int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
+  using Cfg = Config<D, BN>;
+  const size_t smem = Cfg::smem_bytes(a.n);
+  if (smem > static_cast<size_t>(kMaxDynSmem)) {
+    err = "n too large for the forward step table at this key block";
+    return -2;
+  }
+  const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;
+  CUtensorMap tq, tk, tv, to;
+  constexpr uint32_t bc = RowLayout<D>::kBoxCols;
+  if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, kRowsPerTile, bc) ||
+      !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, BN, bc) ||
+      !encode_tile_map(&tv, a.v, kBf16, heads, a.n, D, BN, bc) ||
+      !encode_tile_map(&to, a.o_out, kBf16, heads, a.n, D, kRowsPerTile, bc)) {
+    err = "cuTensorMapEncodeTiled rejected a forward tensor map";
+    return -5;
+  }
+  auto kern = fwd_tc_kernel<kBf16, D, BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) {
+    err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    return -5;
+  }
+  FwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
+              a.lse, a.status};
+  dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads));
+  kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    err = std::string("forward launch: ") + cudaGetErrorString(e);
+    return -5;
+  }
+  return 0;
+}
+
+template <int D>
+int launch_d(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
+  const int bn = a.kv_block == 0 ? 128 : a.kv_block;
+  switch (bn) {
+    case 32: return bf16 ? run<true, D, 32>(a, s, err) : run<false, D, 32>(a, s, err);
+    case 64: return bf16 ? run<true, D, 64>(a, s, err) : run<false, D, 64>(a, s, err);
+    case 128: return bf16 ? run<true, D, 128>(a, s, err) : run<false, D, 128>(a, s, err);
+    default: err = "kv_block must be 0, 32, 64 or 128"; return -2;
+  }
+}
+
+}  // namespace fwd
+}  // namespace ea

@@ -1,0 +1,66 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+namespace ea {
+
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskBitmap = 2 };
+
+// Scalar arguments of the forward kernels (tensor maps travel separately).
+struct FwdParams {
+  int n;
+  float c;
+  int mask_kind;
+  const uint32_t* mask_bits;
+  int64_t mask_row_words;
+  int64_t mask_head_stride_words;
+  float* lse;
+  uint32_t* status;
+};
+
+// Everything a launcher needs; pointers are device pointers.
+struct AttnArgs {
+  int B, H, n, d;
+  float c;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;   // backward: forward output
+  void* o_out;     // forward: output
+  float* lse;      // forward: output; backward: input
+  const void* d_o;
+  void* dq;
+  void* dk;
+  void* dv;
+  int mask_kind;
+  const uint32_t* mask_bits;
+  int64_t mask_row_words;
+  int64_t mask_head_stride_words;
+  int kv_block;
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t* status;
+};
+
+// Each launcher returns 0 or a negative ATTN_ERR_* code and fills `err` on failure.
+int launch_fwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err);
+int launch_bwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err);
+int launch_fwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
+int launch_bwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
+
+// D_i = sum_a dO[i][a] * O[i][a] (float32) for 16-bit or float32 inputs; optionally zeroes a
+// float32 accumulator of `zero_elems` elements.
+int launch_bwd_pre(int dtype, const AttnArgs& a, float* D, float* zero, size_t zero_elems,
+                   cudaStream_t s, std::string& err);
+// dQ = c * acc, rounded to the 16-bit output type.
+int launch_bwd_post(bool bf16, const AttnArgs& a, const float* acc, cudaStream_t s,
+                    std::string& err);
+
+size_t bwd_tc_workspace_bytes(int B, int H, int n, int d);
+size_t bwd_f32_workspace_bytes(int B, int H, int n, int d);
+
+}  // namespace ea

@@ -1,0 +1,132 @@
+/*
+ * exactattn — exact tiled softmax attention on NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * What is computed.  For every head (b, h) and query row i (0-based), with scale c and the
+ * allowed-key set A_i chosen by the mask:
+ *
+ *     s_ij  = c * sum_r Q[i][r] * K[j][r]            (j in A_i)
+ *     LSE_i = m_i + ln( sum_{j in A_i} exp(s_ij - m_i) ),  m_i = max_{j in A_i} s_ij
+ *     O_i   = sum_{j in A_i} exp(s_ij - LSE_i) * V_j
+ *
+ * This is the masked scaled dot-product attention of "Exact tiled attention and
+ * memory-aware differentiation" (definition of the stable summary; exactness theorem), with
+ * the two retained row statistics (m_i, l_i) kept as the single number LSE_i.  The forward
+ * streams key/value blocks past an on-chip tile of query rows and updates the running
+ * maximum, normaliser and weighted value sum, rescaling older partial sums by e^(m - m')
+ * (same page, tiled forward; "The Arithmetic of Intelligence", chapter 12, streaming
+ * softmax).  It never forms the n x n score matrix and writes only O and LSE.
+ *
+ * The backward recomputes each score and probability block from Q, K and the saved LSE
+ * (same page, reverse procedure): with G = dO,
+ *     D_i   = sum_a G[i][a] * O[i][a]
+ *     p_ij  = exp(s_ij - LSE_i),   g_ij = p_ij * (G_i . V_j - D_i)
+ *     dQ_i  = c * sum_j g_ij K_j,  dK_j = c * sum_i g_ij Q_i,  dV_j = sum_i p_ij G_i
+ * It never reads a stored probability matrix.
+ *
+ * Layout.  Q, K, V, O, dO, dQ, dK, dV are contiguous row-major [B][H][n][d] arrays of the
+ * call's dtype (value dimension v = d).  LSE is [B][H][n] float32 (natural log).  All device
+ * pointers must be 16-byte aligned.  Masks:
+ *   ATTN_MASK_NONE    every key is allowed;
+ *   ATTN_MASK_CAUSAL  key j is allowed for query i iff j <= i;
+ *   ATTN_MASK_BITMAP  caller-owned packed allowed sets: device array of uint32 words, row i of
+ *                     head bh starts at word  bh * mask_head_stride_words + i * mask_row_words,
+ *                     key j is allowed iff bit (j % 32) of word (j / 32) of that row is set.
+ *                     mask_row_words >= ceil(n / 32); mask_head_stride_words = 0 shares one
+ *                     bitmap across all heads.  The library only reads it.
+ *
+ * Precision.  ATTN_F32 runs on the CUDA cores in float32 throughout.  ATTN_F16 / ATTN_BF16
+ * run on the tcgen05 tensor cores: the 16-bit inputs are multiplied with float32
+ * accumulation, the probabilities are rounded to the input type (nearest-even) before the
+ * P*V product, and O, dQ, dK, dV are rounded to the input type at the end.
+ *
+ * Supported: d in {16, 32, 64, 128}; n >= 1; B * H >= 1; kv_block in {0 (auto), 32, 64, 128}.
+ * The key-block size b only changes the order of floating-point accumulation: every b gives
+ * the same allowed sets and the same result up to rounding.
+ *
+ * Ownership and errors.  The caller allocates every buffer (inputs, outputs, LSE, workspace,
+ * bitmap).  The library allocates no device memory per call and keeps no state between calls
+ * apart from cached function attributes.  Every entry point returns ATTN_OK (0) or a negative
+ * error code and never throws; attn_last_error() gives a message for the calling thread's last
+ * failure.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream).  A row whose allowed set is empty has no defined output (the pages assume every
+ * A_i is nonempty): the library writes O_i = 0, LSE_i = -inf, adds no gradient for that row
+ * and raises ATTN_WARN_EMPTY_ROW in the device status word.
+ */
+#ifndef EXACTATTN_H
+#define EXACTATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTN_F32 = 0, ATTN_F16 = 1, ATTN_BF16 = 2 } attn_dtype;
+typedef enum { ATTN_MASK_NONE = 0, ATTN_MASK_CAUSAL = 1, ATTN_MASK_BITMAP = 2 } attn_mask_kind;
+
+enum {
+  ATTN_OK = 0,
+  ATTN_WARN_EMPTY_ROW = 1,       /* status only: some row had an empty allowed set */
+  ATTN_ERR_INVALID_ARG = -1,     /* null pointer, non-positive size, bad enum */
+  ATTN_ERR_UNSUPPORTED = -2,     /* head dim / key block / dtype combination not built */
+  ATTN_ERR_ALIGNMENT = -3,       /* a device pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE = -4,       /* workspace missing or smaller than attn_bwd_workspace_bytes */
+  ATTN_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed (message has details) */
+  ATTN_ERR_DEVICE_TIMEOUT = -6   /* a bounded in-kernel wait gave up (see attn_device_status) */
+};
+
+/*
+ * Forward pass.  Writes o [B][H][n][d] (dtype) and lse [B][H][n] (float32, natural log).
+ * Definition: the tiled forward procedure of "Exact tiled attention and memory-aware
+ * differentiation"; O_i = z_i / l_i and LSE_i = m_i + ln l_i from the final row summary.
+ *   dtype      ATTN_F32 / ATTN_F16 / ATTN_BF16, the type of q, k, v and o
+ *   B, H, n, d batch, heads, tokens, head dimension
+ *   c          score scale (commonly 1/sqrt(d))
+ *   q, k, v    device inputs, [B][H][n][d]
+ *   mask_kind  ATTN_MASK_NONE / CAUSAL / BITMAP; the three mask_* words are read only for BITMAP
+ *   kv_block   key-block size b (0 = library choice)
+ *   o, lse     device outputs
+ *   stream     cudaStream_t
+ */
+int attn_fwd(int dtype, int B, int H, int n, int d, float c,
+             const void* q, const void* k, const void* v,
+             int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+             int64_t mask_head_stride_words, int kv_block,
+             void* o, float* lse, void* stream);
+
+/* Bytes of device workspace attn_bwd needs for these sizes (float32 D and dQ accumulators). */
+size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int n, int d);
+
+/*
+ * Backward pass (vector-Jacobian product) for upstream d_o = G.  Writes dq, dk, dv
+ * [B][H][n][d] (dtype).  Definition: the reverse procedure of "Exact tiled attention and
+ * memory-aware differentiation", with the retained statistics given as lse (from attn_fwd on
+ * the same q, k, v, c and mask) and delta_i computed from the stored o.
+ *   workspace  device buffer of at least attn_bwd_workspace_bytes(...) bytes, 16-byte aligned;
+ *              the call overwrites it (its contents on entry do not matter)
+ *   Other arguments as for attn_fwd.
+ */
+int attn_bwd(int dtype, int B, int H, int n, int d, float c,
+             const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* d_o,
+             int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+             int64_t mask_head_stride_words, int kv_block,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+             void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the current device.
+ * Returns ATTN_OK, ATTN_WARN_EMPTY_ROW, ATTN_ERR_DEVICE_TIMEOUT (a bounded wait inside a kernel
+ * gave up; the kernel freed its resources and returned without finishing) or ATTN_ERR_CUDA.
+ */
+int attn_device_status(void* stream);
+
+/* Message describing the calling thread's most recent failed call ("" if none). */
+const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACTATTN_H */

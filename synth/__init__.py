@@ -10,6 +10,7 @@ from .inputs import (  # noqa: F401
     draw_head,
     draw_tensor,
     pack_bitmap,
+    random_allowed,
     round_to_dtype,
     workload,
 )

@@ -127,6 +127,15 @@ def bitmap_mask(n: int, seed: int, window: int = 256, block: int = 64,
     return allowed
 
 
+def random_allowed(n: int, seed: int, keep: float = 0.3, diagonal: bool = True) -> np.ndarray:
+    """Boolean ``[n, n]`` allowed sets with iid membership (probability ``keep``)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 29])))
+    a = g.random((n, n)) < keep
+    if diagonal:
+        a[np.arange(n), np.arange(n)] = True
+    return a
+
+
 def pack_bitmap(allowed: np.ndarray, row_words: int | None = None) -> np.ndarray:
     """Pack a boolean ``[rows, n]`` mask into ``[rows, row_words]`` uint32, LSB first."""
     allowed = np.asarray(allowed, dtype=bool)

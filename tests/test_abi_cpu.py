@@ -1,0 +1,89 @@
+"""The C ABI library loads, exports every entry point the header declares, and rejects bad
+arguments on the host (no GPU needed: argument checks run before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "exactattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_io_aware_gb300.build import build
+
+    path = build()
+    import exact_io_aware_gb300 as ea
+
+    return ea.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_device_status",
+                 "attn_last_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _fwd(lib, **kw):
+    args = dict(dtype=2, B=1, H=1, n=128, d=64, c=0.125, q=16, k=32, v=48, mask=0, bits=0,
+                row_words=0, head_stride=0, kvb=0, o=64, lse=80, stream=0)
+    args.update(kw)
+    vp = ctypes.c_void_p
+    return lib.attn_fwd(args["dtype"], args["B"], args["H"], args["n"], args["d"], args["c"],
+                        vp(args["q"]), vp(args["k"]), vp(args["v"]), args["mask"], vp(args["bits"]),
+                        args["row_words"], args["head_stride"], args["kvb"], vp(args["o"]),
+                        vp(args["lse"]), vp(args["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), -1),
+    (dict(n=0), -1),
+    (dict(B=-1), -1),
+    (dict(d=48), -2),
+    (dict(d=256), -2),
+    (dict(kvb=96), -2),
+    (dict(B=300, H=300), -2),
+    (dict(q=0), -1),
+    (dict(o=0), -1),
+    (dict(lse=0), -1),
+    (dict(q=18), -3),
+    (dict(o=72), -3),
+    (dict(lse=82), -3),
+    (dict(mask=5), -1),
+    (dict(mask=2, bits=0), -1),
+    (dict(mask=2, bits=16, row_words=3), -1),
+    (dict(mask=2, bits=18, row_words=4), -3),
+    (dict(mask=2, bits=16, row_words=4, head_stride=-1), -1),
+])
+def test_forward_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+    assert lib.attn_last_error().decode() != ""
+
+
+def test_backward_workspace_check_on_host(lib):
+    need = lib.attn_bwd_workspace_bytes(2, 2, 3, 1000, 64)
+    rows = 2 * 3 * 1000
+    assert need >= rows * 4 + rows * 64 * 4
+    assert lib.attn_bwd_workspace_bytes(0, 2, 3, 1000, 64) >= rows * 4
+    assert lib.attn_bwd_workspace_bytes(2, 0, 3, 1000, 64) == 0
+    vp = ctypes.c_void_p
+    rc = lib.attn_bwd(2, 2, 3, 1000, 64, 0.125, vp(16), vp(32), vp(48), vp(64), vp(80), vp(96),
+                      0, vp(0), 0, 0, 0, vp(112), vp(128), vp(144), vp(160), need - 1, vp(0))
+    assert rc == -4
+    rc = lib.attn_bwd(2, 2, 3, 1000, 64, 0.125, vp(16), vp(32), vp(48), vp(64), vp(80), vp(0),
+                      0, vp(0), 0, 0, 0, vp(112), vp(128), vp(144), vp(160), need, vp(0))
+    assert rc == -1
