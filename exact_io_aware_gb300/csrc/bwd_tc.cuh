@@ -1,0 +1,550 @@
+// Backward pass of exact tiled softmax attention on the tcgen05 tensor cores (fp16 / bf16).
+//
+// Follows the reverse procedure of "Exact tiled attention and memory-aware differentiation":
+// every score block is recomputed from Q and K, p_ij = exp(s_ij - LSE_i) uses the retained row
+// statistic, g_ij = p_ij (dO_i . V_j - D_i) with D_i = dO_i . O_i, and
+//   dV_j += p_ij dO_i,   dK_j += c g_ij Q_i,   dQ_i += c g_ij K_j.
+// No probability matrix is ever stored.
+//
+// One CTA owns a tile of 128 keys of one head and walks the query blocks that can reach it
+// (all of them, those at or after the diagonal under the causal mask, or the nonempty ones
+// under a bitmap).  Per query block of BQ rows:
+//   Sᵀ  = K Qᵀ          (tensor memory, one key per lane)
+//   Pᵀ  = exp2(Sᵀ c log2e - LSE log2e)           softmax warps, written back as 16-bit
+//   dPᵀ = V dOᵀ
+//   dSᵀ = Pᵀ (dPᵀ - D)                           softmax warps, to tensor and shared memory
+//   dV += Pᵀ dO,  dK += dSᵀ Q                    (A operand read from tensor memory)
+//   dQ  = dS K   (d <= 64)  or  dQᵀ = Kᵀ dSᵀ (d = 128, so the 128-lane accumulator holds d)
+// and dQ is added into a float32 accumulator in global memory; dK and dV stay in tensor memory
+// until the last block.  Roles:
+//   warps 0-3  softmax (P and dS)            warps 4-7  dQ reduction and dK/dV epilogue
+//   warp  8    TMA producer (K, V once; Q, dO per block through an NS-stage ring)
+//   warp  9    TMEM allocator and MMA issuer
+// With d = 128 a block has 64 queries and two S buffers, so S of the next block is computed
+// while the softmax warps still work on the current one.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "tile.cuh"
+
+namespace ea {
+namespace bwd {
+
+constexpr int kKeys = 128;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
+
+struct BwdParams {
+  int n;
+  float c;
+  int mask_kind;
+  const uint32_t* mask_bits;
+  int64_t mask_row_words;
+  int64_t mask_head_stride_words;
+  const float* lse;
+  const float* Dv;
+  float* dq_acc;
+  uint32_t* status;
+};
+
+__host__ __device__ constexpr int pad32(int x) { return x < 32 ? 32 : x; }
+
+template <int D>
+struct Config {
+  static constexpr bool kTr = D == 128;  // dQᵀ = Kᵀ dSᵀ
+  static constexpr int BQ = kTr ? 64 : 128;
+  using TK = Tile<kKeys, D>;   // K, V (and dK, dV staging)
+  using TQ = Tile<BQ, D>;      // Q, dO stages
+  using TS = Tile<kKeys, BQ>;  // dSᵀ: rows = keys, cols = queries
+  static constexpr int kDqCols = pad32(kTr ? BQ : D);
+  static constexpr int kTwoS = 2 * BQ + BQ + kDqCols + 2 * pad32(D);
+  static constexpr int NSB = kTwoS <= 512 ? 2 : 1;
+  // tensor-memory columns
+  static constexpr int kColS = 0;  // S buffer b at b * BQ
+  static constexpr int kColDP = NSB * BQ;
+  static constexpr int kColDV = kColDP + BQ;
+  static constexpr int kColDK = kColDV + pad32(D);
+  static constexpr int kColDQ = kColDK + pad32(D);
+  static constexpr int kTmemCols = kColDQ + kDqCols;
+  static_assert(kTmemCols <= 512, "tensor memory overflow");
+  static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
+  // shared memory
+  static constexpr int kBudget = 227 * 1024 - 2048;
+  static constexpr int kFixed = 2 * TK::kBytes + 2 * TS::kBytes + 4 * BQ * 4;
+  static constexpr int kStage = 2 * TQ::kBytes;
+  static constexpr int kMaxStepBytes = 8 * 1024;
+  static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes) / kStage;
+  static constexpr int NS = kFit > 4 ? 4 : kFit;
+  static_assert(NS >= 2, "need two query stages");
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + TK::kBytes;
+  static constexpr int kOffDS = kOffV + TK::kBytes;
+  static constexpr int kOffQ = kOffDS + 2 * TS::kBytes;
+  static constexpr int kOffG = kOffQ + NS * TQ::kBytes;
+  static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [2][BQ] LSE (log2 units)
+  static constexpr int kOffD = kOffL + 2 * BQ * 4;       // [2][BQ] D
+  static constexpr int kOffSteps = kOffD + 2 * BQ * 4;
+  static size_t smem_bytes(int n) {
+    const int nqb = (n + BQ - 1) / BQ;
+    return 1024 + kOffSteps + 4 * static_cast<size_t>(nqb);
+  }
+};
+
+struct Barriers {
+  uint64_t kv_full;
+  uint64_t qdo_full[4], qdo_empty[4];
+  uint64_t s_full[2];
+  uint64_t p_full, dp_full, ds_full;
+  uint64_t dss_free[2];
+  uint64_t dq_full, dq_free;
+  uint64_t kv_done;
+  uint32_t tmem_base;
+  uint32_t nsteps;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+  if constexpr (kBf16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    float2 f = __half22float2(h);
+    lo = f.x;
+    hi = f.y;
+  }
+}
+
+template <bool kBf16, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                  const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                  BwdParams p) {
+  using C = Config<D>;
+  using TK = typename C::TK;
+  using TQ = typename C::TQ;
+  using TS = typename C::TS;
+  constexpr int BQ = C::BQ;
+  constexpr int NS = C::NS;
+  constexpr int NSB = C::NSB;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sDS = smem + C::kOffDS;
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sG = smem + C::kOffG;
+  float* sL = reinterpret_cast<float*>(smem + C::kOffL);
+  float* sD = reinterpret_cast<float*>(smem + C::kOffD);
+  uint32_t* steps = reinterpret_cast<uint32_t*>(smem + C::kOffSteps);
+  __shared__ Barriers bars;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int n = p.n;
+  const int bh = blockIdx.y;
+  const int key0 = blockIdx.x * kKeys;
+  const int nqb = (n + BQ - 1) / BQ;
+
+  // ---------------------------------------------------------------- prologue
+  if (tid == 0) {
+    mbar_init(&bars.kv_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars.qdo_full[s], 1);
+      mbar_init(&bars.qdo_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.s_full[b], 1);
+      mbar_init(&bars.dss_free[b], 1);
+    }
+    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ds_full, 4);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.dq_free, 4);
+    mbar_init(&bars.kv_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
+
+  // Classify each query block against this key tile: skip / full / partial.
+  for (int i = tid; i < nqb; i += kThreads) steps[i] = 0;
+  __syncthreads();
+  const bool key_tail = key0 + kKeys > n;
+  if (p.mask_kind == kMaskBitmap) {
+    if (tid < 256) {
+      const int nwords = (min(key0 + kKeys, n) - key0 + 31) / 32;
+      for (int q0 = 0; q0 < n; q0 += 256) {
+        const int q = q0 + tid;
+        bool any = false, all = true;
+        if (q < n) {
+          const uint32_t* row = p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
+                                static_cast<int64_t>(q) * p.mask_row_words + key0 / 32;
+          for (int w = 0; w < nwords; ++w) {
+            const int nk = n - (key0 + 32 * w);
+            const uint32_t live = nk >= 32 ? 0xFFFFFFFFu : ((1u << nk) - 1u);
+            const uint32_t bits = __ldg(row + w) & live;
+            any |= bits != 0;
+            all &= bits == live;
+          }
+        }
+        // a warp's 32 rows lie in one query block (BQ is a multiple of 32)
+        const bool wany = __any_sync(0xFFFFFFFFu, any);
+        const bool wall = __all_sync(0xFFFFFFFFu, all);
+        if (lane == 0 && q0 + warp * 32 < n) {
+          const uint32_t bits = (wany ? 1u : 0u) | (wall ? 0u : 2u);
+          if (bits) atomicOr(&steps[(q0 + warp * 32) / BQ], bits);
+        }
+      }
+    }
+  } else {
+    for (int i = tid; i < nqb; i += kThreads) {
+      const int q0 = i * BQ;
+      const int qlast = min(q0 + BQ, n) - 1;
+      bool any = true, all = true;
+      if (p.mask_kind == kMaskCausal) {
+        any = qlast >= key0;
+        all = q0 >= key0 + kKeys - 1;
+      }
+      steps[i] = any ? (1u | (all ? 0u : 2u)) : 0u;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int ns = 0;
+    for (int i = 0; i < nqb; ++i) {
+      const uint32_t b = steps[i];
+      if (!(b & 1u)) continue;
+      const bool tail = key_tail || (i + 1) * BQ > n;
+      const uint32_t cls = ((b & 2u) || tail) ? kPartial : kFull;
+      steps[ns++] = static_cast<uint32_t>(i) | (cls << 16);
+    }
+    bars.nsteps = ns;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int nsteps = bars.nsteps;
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_g);
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * TK::kBytes);
+#pragma unroll
+      for (int b = 0; b < TK::L::kBoxes; ++b) {
+        tma_load_3d(sK + b * TK::kBoxBytes, &tm_k, &bars.kv_full, b * TK::L::kBoxCols, key0, bh);
+        tma_load_3d(sV + b * TK::kBoxBytes, &tm_v, &bars.kv_full, b * TK::L::kBoxCols, key0, bh);
+      }
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % NS;
+        const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
+        if (!mbar_wait(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
+        mbar_arrive_expect_tx(&bars.qdo_full[s], 2 * TQ::kBytes);
+#pragma unroll
+        for (int b = 0; b < TQ::L::kBoxes; ++b) {
+          tma_load_3d(sQ + s * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.qdo_full[s],
+                      b * TQ::L::kBoxCols, q0, bh);
+          tma_load_3d(sG + s * TQ::kBytes + b * TQ::kBoxBytes, &tm_g, &bars.qdo_full[s],
+                      b * TQ::L::kBoxCols, q0, bh);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);   // Sᵀ, dPᵀ
+      constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dV, dK
+      constexpr uint32_t id_q = C::kTr ? idesc_f16(D, BQ, kBf16 ? 1 : 0, 1, 1)
+                                       : idesc_f16(BQ, D, kBf16 ? 1 : 0, 1, 1);
+      const uint32_t sk = smem_u32(sK), sv = smem_u32(sV);
+      bool ok = mbar_wait(&bars.kv_full, 0, p.status, 22);
+      auto wait_qdo = [&](int i) -> bool {
+        return mbar_wait(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
+      };
+      auto issue_s = [&](int i) {
+        const uint32_t qb = smem_u32(sQ + (i % NS) * TQ::kBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColS + (i % NSB) * BQ, TK::desc_k(sk, kk), TQ::desc_k(qb, kk), id_s,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&bars.s_full[i % NSB]);
+      };
+      auto issue_dp = [&](int i) {
+        const uint32_t gb = smem_u32(sG + (i % NS) * TQ::kBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColDP, TK::desc_k(sv, kk), TQ::desc_k(gb, kk), id_s, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.dp_full);
+      };
+      if (ok && nsteps > 0) {
+        ok = wait_qdo(0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
+        }
+      }
+      for (int i = 0; i < nsteps && ok; ++i) {
+        const int s = i % NS;
+        const uint32_t qb = smem_u32(sQ + s * TQ::kBytes);
+        const uint32_t gb = smem_u32(sG + s * TQ::kBytes);
+        if (NSB == 2 && i + 1 < nsteps) {
+          ok = wait_qdo(i + 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        ok = mbar_wait(&bars.p_full, i & 1, p.status, 24);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + (i % NSB) * BQ + kk * 8, TQ::desc_mn(gb, kk),
+                 id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+        ok = mbar_wait(&bars.ds_full, i & 1, p.status, 25);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, TQ::desc_mn(qb, kk), id_kv,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        ok = mbar_wait(&bars.dq_free, (i & 1) ^ 1, p.status, 26);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t dsb = smem_u32(sDS + (i & 1) * TS::kBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          if constexpr (C::kTr)
+            mma_ss(tmem + C::kColDQ, TK::desc_mn(sk, kk), TS::desc_mn(dsb, kk), id_q,
+                   kk > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + C::kColDQ, TS::desc_mn(dsb, kk), TK::desc_mn(sk, kk), id_q,
+                   kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars.dq_full);
+        mma_commit(&bars.qdo_empty[s]);
+        mma_commit(&bars.dss_free[i & 1]);
+        if (i + 1 < nsteps) {
+          if (NSB == 1) {
+            ok = wait_qdo(i + 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(i + 1);
+          }
+          issue_dp(i + 1);
+        }
+      }
+      mma_commit(&bars.kv_done);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- softmax: P and dS
+    const int r = tid;  // key row within the tile = TMEM lane
+    const int j = key0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.c * 1.4426950408889634f;
+    const uint32_t* bits_base =
+        p.mask_kind == kMaskBitmap
+            ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words + (j < n ? j : 0) / 32
+            : nullptr;
+    const float* lse_h = p.lse + static_cast<int64_t>(bh) * n;
+    const float* d_h = p.Dv + static_cast<int64_t>(bh) * n;
+    bool ok = true;
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
+      const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
+      float* L = sL + (i & 1) * BQ;
+      float* Dd = sD + (i & 1) * BQ;
+      for (int t = r; t < BQ; t += 128) {
+        const int q = q0 + t;
+        const float lv = q < n ? __ldg(lse_h + q) : -INFINITY;
+        L[t] = lv == -INFINITY ? INFINITY : lv * 1.4426950408889634f;
+        Dd[t] = q < n ? __ldg(d_h + q) : 0.0f;
+      }
+      named_barrier(1, 128);
+      ok = mbar_wait(&bars.s_full[i % NSB], (i / NSB) & 1, p.status, 27);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + C::kColS + (i % NSB) * BQ + lane_off;
+      const uint32_t tP = tmem + C::kColDP + lane_off;
+#pragma unroll
+      for (int c0 = 0; c0 < BQ; c0 += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS + c0, rr);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float pr[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int t = c0 + 2 * k + h;
+            float v = ex2(__uint_as_float(rr[2 * k + h]) * sl2 - L[t]);
+            if (partial) {
+              const int q = q0 + t;
+              bool allowed = q < n && j < n;
+              if (p.mask_kind == kMaskCausal)
+                allowed = allowed && j <= q;
+              else if (p.mask_kind == kMaskBitmap)
+                allowed = allowed &&
+                          ((__ldg(bits_base + static_cast<int64_t>(q) * p.mask_row_words) >> (j & 31)) & 1u);
+              if (!allowed) v = 0.0f;
+            }
+            pr[h] = v;
+          }
+          pk[k] = pack2<kBf16>(pr[0], pr[1]);
+        }
+        tmem_st16(tS + c0 / 2, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full);
+
+      ok = mbar_wait(&bars.dp_full, i & 1, p.status, 28);
+      if (ok && i >= 2) ok = mbar_wait(&bars.dss_free[i & 1], ((i >> 1) & 1) ^ 1, p.status, 29);
+      if (!ok) break;
+      tc_fence_after();
+      uint8_t* ds_tile = sDS + (i & 1) * TS::kBytes;
+#pragma unroll
+      for (int c0 = 0; c0 < BQ; c0 += 32) {
+        uint32_t dp[32];
+        uint32_t pp[16];
+        tmem_ld32(tP + c0, dp);
+        tmem_ld16(tS + c0 / 2, pp);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float p0, p1;
+          unpack2<kBf16>(pp[k], p0, p1);
+          const float g0 = p0 * (__uint_as_float(dp[2 * k]) - Dd[c0 + 2 * k]);
+          const float g1 = p1 * (__uint_as_float(dp[2 * k + 1]) - Dd[c0 + 2 * k + 1]);
+          pk[k] = pack2<kBf16>(g0, g1);
+        }
+        tmem_st16(tP + c0 / 2, pk);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(ds_tile + TS::offset(r, c0 + 8 * u)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ds_full);
+    }
+  } else {
+    // ---------------------------------------------------------------- dQ reduction, epilogue
+    const int quad = warp - 4;
+    const int r = quad * 32 + lane;  // TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    float* acc = p.dq_acc + static_cast<int64_t>(bh) * n * D;
+    bool ok = true;
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
+      ok = mbar_wait(&bars.dq_full, i & 1, p.status, 30);
+      if (!ok) break;
+      tc_fence_after();
+      if constexpr (C::kTr) {
+        // lane = column a of dQ (a < D = 128), columns = the block's queries
+#pragma unroll
+        for (int c0 = 0; c0 < BQ; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tmem + C::kColDQ + lane_off + c0, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int q = q0 + c0 + k;
+            if (q < n) atomicAdd(acc + static_cast<int64_t>(q) * D + r, __uint_as_float(rr[k]));
+          }
+        }
+      } else {
+        // lane = query of the block, columns = dQ columns
+        const int q = q0 + r;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t rr[16];
+          tmem_ld16(tmem + C::kColDQ + lane_off + c0, rr);
+          tmem_wait_ld();
+          if (q < n) {
+            float4* dst = reinterpret_cast<float4*>(acc + static_cast<int64_t>(q) * D + c0);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              atomicAdd(dst + u, make_float4(__uint_as_float(rr[4 * u]), __uint_as_float(rr[4 * u + 1]),
+                                             __uint_as_float(rr[4 * u + 2]), __uint_as_float(rr[4 * u + 3])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.dq_free);
+    }
+    // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
+    if (ok) ok = mbar_wait(&bars.kv_done, 0, p.status, 31);
+    tc_fence_after();
+    if (ok) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t rv[16], rk[16];
+        if (nsteps > 0) {
+          tmem_ld16(tmem + C::kColDV + lane_off + c0, rv);
+          tmem_ld16(tmem + C::kColDK + lane_off + c0, rk);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) rv[k] = rk[k] = 0u;
+        }
+        uint32_t pv[8], pkk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          pv[k] = pack2<kBf16>(__uint_as_float(rv[2 * k]), __uint_as_float(rv[2 * k + 1]));
+          pkk[k] = pack2<kBf16>(p.c * __uint_as_float(rk[2 * k]), p.c * __uint_as_float(rk[2 * k + 1]));
+        }
+        *reinterpret_cast<uint4*>(sV + TK::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+        *reinterpret_cast<uint4*>(sV + TK::offset(r, c0 + 8)) = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+        *reinterpret_cast<uint4*>(sK + TK::offset(r, c0)) = make_uint4(pkk[0], pkk[1], pkk[2], pkk[3]);
+        *reinterpret_cast<uint4*>(sK + TK::offset(r, c0 + 8)) =
+            make_uint4(pkk[4], pkk[5], pkk[6], pkk[7]);
+      }
+    }
+    fence_proxy_async_smem();
+    named_barrier(2, 128);
+    if (ok && r == 0) {
+#pragma unroll
+      for (int b = 0; b < TK::L::kBoxes; ++b) {
+        tma_store_3d(&tm_dk, sK + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
+        tma_store_3d(&tm_dv, sV + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
+      }
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemAlloc);
+  }
+}
+
+}  // namespace bwd
+}  // namespace ea

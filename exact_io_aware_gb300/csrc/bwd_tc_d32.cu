@@ -1,0 +1,9 @@
+// tcgen05 backward kernels for head dimension 32.
+#include "bwd_tc_launch.cuh"
+
+namespace ea {
+int launch_bwd_tc_d32(bool bf16, const AttnArgs& a, float* Dv, float* acc, cudaStream_t s,
+                      std::string& err) {
+  return bf16 ? bwd::run<true, 32>(a, Dv, acc, s, err) : bwd::run<false, 32>(a, Dv, acc, s, err);
+}
+}  // namespace ea
