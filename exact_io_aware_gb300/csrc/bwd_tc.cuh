@@ -72,10 +72,11 @@ struct Config {
   static constexpr int kTmemCols = kColDQ + kDqCols;
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
-  // shared memory
+  using TDQ = F32Tile<BQ, D>;  // float32 dQ block staged for the TMA reduce-add
+  // shared memory: K, V, two dSᵀ buffers, dQ staging, then NS stages of (Q, dO, LSE, D)
   static constexpr int kBudget = 227 * 1024 - 2048;
-  static constexpr int kFixed = 2 * TK::kBytes + 2 * TS::kBytes + 4 * BQ * 4;
-  static constexpr int kStage = 2 * TQ::kBytes;
+  static constexpr int kFixed = 2 * TK::kBytes + 2 * TS::kBytes + TDQ::kBytes;
+  static constexpr int kStage = 2 * TQ::kBytes + 2 * BQ * 4;
   static constexpr int kMaxStepBytes = 8 * 1024;
   static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes) / kStage;
   static constexpr int NS = kFit > 4 ? 4 : kFit;
@@ -83,11 +84,12 @@ struct Config {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + TK::kBytes;
   static constexpr int kOffDS = kOffV + TK::kBytes;
-  static constexpr int kOffQ = kOffDS + 2 * TS::kBytes;
+  static constexpr int kOffDQ = kOffDS + 2 * TS::kBytes;
+  static constexpr int kOffQ = kOffDQ + TDQ::kBytes;
   static constexpr int kOffG = kOffQ + NS * TQ::kBytes;
-  static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [2][BQ] LSE (log2 units)
-  static constexpr int kOffD = kOffL + 2 * BQ * 4;       // [2][BQ] D
-  static constexpr int kOffSteps = kOffD + 2 * BQ * 4;
+  static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [NS][BQ] LSE (log2 units)
+  static constexpr int kOffD = kOffL + NS * BQ * 4;      // [NS][BQ] D
+  static constexpr int kOffSteps = kOffD + NS * BQ * 4;
   static size_t smem_bytes(int n) {
     const int nqb = (n + BQ - 1) / BQ;
     return 1024 + kOffSteps + 4 * static_cast<size_t>(nqb);
@@ -96,9 +98,9 @@ struct Config {
 
 struct Barriers {
   uint64_t kv_full;
-  uint64_t qdo_full[4], qdo_empty[4];
+  uint64_t qdo_full[4], qdo_empty[4], ld_full[4];
   uint64_t s_full[2];
-  uint64_t p_full, dp_full, ds_full;
+  uint64_t p_full[2], dp_full, ds_full;
   uint64_t dss_free[2];
   uint64_t dq_full, dq_free;
   uint64_t kv_done;
@@ -132,11 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                  BwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_dq, BwdParams p) {
   using C = Config<D>;
   using TK = typename C::TK;
   using TQ = typename C::TQ;
   using TS = typename C::TS;
+  using TDQ = typename C::TDQ;
   constexpr int BQ = C::BQ;
   constexpr int NS = C::NS;
   constexpr int NSB = C::NSB;
@@ -146,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint8_t* sDS = smem + C::kOffDS;
+  uint8_t* sDQ = smem + C::kOffDQ;
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sG = smem + C::kOffG;
   float* sL = reinterpret_cast<float*>(smem + C::kOffL);
@@ -167,12 +171,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars.qdo_full[s], 1);
       mbar_init(&bars.qdo_empty[s], 1);
+      mbar_init(&bars.ld_full[s], 32);
     }
+    // p_full is per S buffer: with two buffers a fast softmax warp may publish P of the next
+    // block before a slow warp has published P of this one, and one shared barrier would then
+    // count that early arrival towards the wrong phase.
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.dss_free[b], 1);
+      mbar_init(&bars.p_full[b], 4);
     }
-    mbar_init(&bars.p_full, 4);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_full, 4);
     mbar_init(&bars.dq_full, 1);
@@ -243,7 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
 
   if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- producer warp
+    // Lane 0 issues the TMA loads; all lanes stage each block's LSE (log2 units, +inf for
+    // rows past n or with an empty allowed set) and D into shared memory.
+    const float* lse_h = p.lse + static_cast<int64_t>(bh) * n;
+    const float* d_h = p.Dv + static_cast<int64_t>(bh) * n;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_g);
@@ -253,10 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sK + b * TK::kBoxBytes, &tm_k, &bars.kv_full, b * TK::L::kBoxCols, key0, bh);
         tma_load_3d(sV + b * TK::kBoxBytes, &tm_v, &bars.kv_full, b * TK::L::kBoxCols, key0, bh);
       }
-      for (int i = 0; i < nsteps; ++i) {
-        const int s = i % NS;
-        const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
-        if (!mbar_wait(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
+    }
+    for (int i = 0; i < nsteps; ++i) {
+      const int s = i % NS;
+      const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
+      if (!mbar_wait(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bars.qdo_full[s], 2 * TQ::kBytes);
 #pragma unroll
         for (int b = 0; b < TQ::L::kBoxes; ++b) {
@@ -266,6 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       b * TQ::L::kBoxCols, q0, bh);
         }
       }
+      for (int t = lane; t < BQ; t += 32) {
+        const int q = q0 + t;
+        const float lv = q < n ? __ldg(lse_h + q) : -INFINITY;
+        sL[s * BQ + t] = lv == -INFINITY ? INFINITY : lv * 1.4426950408889634f;
+        sD[s * BQ + t] = q < n ? __ldg(d_h + q) : 0.0f;
+      }
+      mbar_arrive(&bars.ld_full[s]);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
@@ -302,6 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_dp(0);
         }
       }
+      // Order per block i: [S_{i+1}], dV_i, dK_i, [S_{i+1}], dP_{i+1}, dQ_i.  dP_{i+1} goes
+      // before dQ_i so the softmax warps can start dS_{i+1} while dQ_i is reduced.
       for (int i = 0; i < nsteps && ok; ++i) {
         const int s = i % NS;
         const uint32_t qb = smem_u32(sQ + s * TQ::kBytes);
@@ -312,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(i + 1);
         }
-        ok = mbar_wait(&bars.p_full, i & 1, p.status, 24);
+        ok = mbar_wait(&bars.p_full[i % NSB], (i / NSB) & 1, p.status, 24);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -326,6 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BQ / 16; ++kk)
           mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, TQ::desc_mn(qb, kk), id_kv,
                  (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.qdo_empty[s]);
+        if (i + 1 < nsteps) {
+          if (NSB == 1) {
+            ok = wait_qdo(i + 1);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(i + 1);
+          }
+          issue_dp(i + 1);
+        }
         ok = mbar_wait(&bars.dq_free, (i & 1) ^ 1, p.status, 26);
         if (!ok) break;
         tc_fence_after();
@@ -340,17 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.dq_full);
-        mma_commit(&bars.qdo_empty[s]);
         mma_commit(&bars.dss_free[i & 1]);
-        if (i + 1 < nsteps) {
-          if (NSB == 1) {
-            ok = wait_qdo(i + 1);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(i + 1);
-          }
-          issue_dp(i + 1);
-        }
       }
       mma_commit(&bars.kv_done);
     }
@@ -364,21 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.mask_kind == kMaskBitmap
             ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words + (j < n ? j : 0) / 32
             : nullptr;
-    const float* lse_h = p.lse + static_cast<int64_t>(bh) * n;
-    const float* d_h = p.Dv + static_cast<int64_t>(bh) * n;
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
       const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
-      float* L = sL + (i & 1) * BQ;
-      float* Dd = sD + (i & 1) * BQ;
-      for (int t = r; t < BQ; t += 128) {
-        const int q = q0 + t;
-        const float lv = q < n ? __ldg(lse_h + q) : -INFINITY;
-        L[t] = lv == -INFINITY ? INFINITY : lv * 1.4426950408889634f;
-        Dd[t] = q < n ? __ldg(d_h + q) : 0.0f;
-      }
-      named_barrier(1, 128);
+      const float* L = sL + (i % NS) * BQ;
+      const float* Dd = sD + (i % NS) * BQ;
+      ok = mbar_wait(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
+      if (!ok) break;
       ok = mbar_wait(&bars.s_full[i % NSB], (i / NSB) & 1, p.status, 27);
       if (!ok) break;
       tc_fence_after();
@@ -416,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full);
+      if (lane == 0) mbar_arrive(&bars.p_full[i % NSB]);
 
       ok = mbar_wait(&bars.dp_full, i & 1, p.status, 28);
       if (ok && i >= 2) ok = mbar_wait(&bars.dss_free[i & 1], ((i >> 1) & 1) ^ 1, p.status, 29);
@@ -456,13 +472,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp - 4;
     const int r = quad * 32 + lane;  // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    float* acc = p.dq_acc + static_cast<int64_t>(bh) * n * D;
+    // Each block's dQ leaves tensor memory through a swizzled float32 staging tile and one
+    // TMA reduce-add per 32-column box into the float32 accumulator (rows past n are dropped
+    // by the tensor map).  Tensor memory is released before the shared-memory copy is done.
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
       ok = mbar_wait(&bars.dq_full, i & 1, p.status, 30);
       if (!ok) break;
       tc_fence_after();
+      if (i > 0) {
+        if (r == 0) tma_store_wait_read();  // the previous block's reduce has read the tile
+        named_barrier(2, 128);
+      }
       if constexpr (C::kTr) {
         // lane = column a of dQ (a < D = 128), columns = the block's queries
 #pragma unroll
@@ -471,32 +493,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + C::kColDQ + lane_off + c0, rr);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int q = q0 + c0 + k;
-            if (q < n) atomicAdd(acc + static_cast<int64_t>(q) * D + r, __uint_as_float(rr[k]));
-          }
+          for (int k = 0; k < 32; ++k)
+            *reinterpret_cast<uint32_t*>(sDQ + TDQ::offset(c0 + k, r)) = rr[k];
         }
       } else {
         // lane = query of the block, columns = dQ columns
-        const int q = q0 + r;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
           uint32_t rr[16];
           tmem_ld16(tmem + C::kColDQ + lane_off + c0, rr);
           tmem_wait_ld();
-          if (q < n) {
-            float4* dst = reinterpret_cast<float4*>(acc + static_cast<int64_t>(q) * D + c0);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              atomicAdd(dst + u, make_float4(__uint_as_float(rr[4 * u]), __uint_as_float(rr[4 * u + 1]),
-                                             __uint_as_float(rr[4 * u + 2]), __uint_as_float(rr[4 * u + 3])));
-          }
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(sDQ + TDQ::offset(r, c0 + 4 * u)) =
+                make_uint4(rr[4 * u], rr[4 * u + 1], rr[4 * u + 2], rr[4 * u + 3]);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.dq_free);
+      fence_proxy_async_smem();
+      named_barrier(2, 128);
+      if (r == 0) {
+#pragma unroll
+        for (int b = 0; b < TDQ::kBoxes; ++b)
+          tma_reduce_add_3d(&tm_dq, sDQ + b * TDQ::kBoxBytes, b * TDQ::kBoxCols, q0, bh);
+        tma_store_commit();
+      }
     }
+    if (r == 0) tma_store_wait_all();
     // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
     if (ok) ok = mbar_wait(&bars.kv_done, 0, p.status, 31);
     tc_fence_after();

@@ -18,13 +18,14 @@ int run(const AttnArgs& a, float* Dv, float* acc, cudaStream_t s, std::string& e
   }
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;
   constexpr uint32_t bc = RowLayout<D>::kBoxCols;
-  CUtensorMap tq, tk, tv, tg, tdk, tdv;
+  CUtensorMap tq, tk, tv, tg, tdk, tdv, tdq;
   if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, Cfg::BQ, bc) ||
       !encode_tile_map(&tg, a.d_o, kBf16, heads, a.n, D, Cfg::BQ, bc) ||
       !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, kKeys, bc) ||
       !encode_tile_map(&tv, a.v, kBf16, heads, a.n, D, kKeys, bc) ||
       !encode_tile_map(&tdk, a.dk, kBf16, heads, a.n, D, kKeys, bc) ||
-      !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, D, kKeys, bc)) {
+      !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, D, kKeys, bc) ||
+      !encode_f32_map(&tdq, acc, heads, a.n, D, Cfg::BQ, Cfg::TDQ::kBoxCols)) {
     err = "cuTensorMapEncodeTiled rejected a backward tensor map";
     return -5;
   }
@@ -38,7 +39,7 @@ int run(const AttnArgs& a, float* Dv, float* acc, cudaStream_t s, std::string& e
   BwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
               a.lse, Dv, acc, a.status};
   dim3 grid((a.n + kKeys - 1) / kKeys, static_cast<unsigned>(heads));
-  kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, tg, tdk, tdv, p);
+  kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, tg, tdk, tdv, tdq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("backward launch: ") + cudaGetErrorString(e);

@@ -109,6 +109,20 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_
       : "memory");
 }
 
+// 3-D tiled reduce-add of one box from shared memory into global memory (bulk-group).
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* smem_src, int x,
+                                                  int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -58,4 +58,20 @@ struct Tile {
   }
 };
 
+// A float32 tile of R rows x C columns staged for TMA: boxes of R rows x min(C, 32) columns
+// (rows of 64 or 128 bytes) with the matching swizzle, stored back to back.
+template <int R, int C>
+struct F32Tile {
+  static constexpr int kBoxCols = C < 32 ? C : 32;
+  static constexpr int kRowBytes = kBoxCols * 4;
+  static constexpr int kBoxes = C / kBoxCols;
+  static constexpr int kBoxBytes = R * kRowBytes;
+  static constexpr int kBytes = kBoxBytes * kBoxes;
+  static_assert(kRowBytes == 64 || kRowBytes == 128, "fp32 tile rows must be 64 or 128 bytes");
+  __host__ __device__ static constexpr uint32_t offset(int r, int c) {
+    const uint32_t a = (c / kBoxCols) * kBoxBytes + r * kRowBytes + (c % kBoxCols) * 4;
+    return a ^ (((a >> 7) & (kRowBytes / 16 - 1)) << 4);
+  }
+};
+
 }  // namespace ea
