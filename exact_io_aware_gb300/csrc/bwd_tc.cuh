@@ -405,28 +405,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t rr[32];
         tmem_ld32(tS + c0, rr);
         tmem_wait_ld();
+        float pv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[k]) * sl2 - L[c0 + k]);
+        // Masking is a separate pass over the chunk so the common (full-block) path above
+        // stays one compact run of instructions.
+        if (partial) {
+          if (p.mask_kind == kMaskBitmap) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int q = q0 + c0 + k;
+              const bool allowed =
+                  q < n && j < n &&
+                  ((__ldg(bits_base + static_cast<int64_t>(q) * p.mask_row_words) >> (j & 31)) & 1u);
+              if (!allowed) pv[k] = 0.0f;
+            }
+          } else {
+            const bool causal = p.mask_kind == kMaskCausal;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int q = q0 + c0 + k;
+              if (q >= n || j >= n || (causal && j > q)) pv[k] = 0.0f;
+            }
+          }
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float pr[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int t = c0 + 2 * k + h;
-            float v = ex2(__uint_as_float(rr[2 * k + h]) * sl2 - L[t]);
-            if (partial) {
-              const int q = q0 + t;
-              bool allowed = q < n && j < n;
-              if (p.mask_kind == kMaskCausal)
-                allowed = allowed && j <= q;
-              else if (p.mask_kind == kMaskBitmap)
-                allowed = allowed &&
-                          ((__ldg(bits_base + static_cast<int64_t>(q) * p.mask_row_words) >> (j & 31)) & 1u);
-              if (!allowed) v = 0.0f;
-            }
-            pr[h] = v;
-          }
-          pk[k] = pack2<kBf16>(pr[0], pr[1]);
-        }
+        for (int k = 0; k < 16; ++k) pk[k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
         tmem_st16(tS + c0 / 2, pk);
       }
       tmem_wait_st();
