@@ -99,7 +99,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -194,7 +194,7 @@ def time_oracle(heads: int):
     return 14.0 * N_TOK * N_TOK * D * heads, dt
 
 
-def cpu_baseline(heads=2):
+def cpu_baseline(heads=24):
     flop, dt = time_oracle(heads)
     return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
             "sample": f"{heads} of {B * H} heads of {WORKLOAD} (n={N_TOK}, d={D}), forward + "
@@ -366,7 +366,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
