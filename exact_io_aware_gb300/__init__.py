@@ -20,7 +20,7 @@ __all__ = [
     "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
-    "attn_device_status", "attn_last_error", "attention",
+    "attn_device_status", "attn_last_error", "attention", "attn_bwd_noalloc",
 ]
 
 ATTN_OK = 0
@@ -153,6 +153,36 @@ def attn_bwd(q, k, v, o, lse, do, c, mask="none", mask_bits=None, mask_head_stri
                            _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits), row_words, hs,
                            int(kv_block), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                            workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, do, c, mask="none", mask_bits=None,
+                     mask_head_stride_words=0, kv_block=0, dq=None, dk=None, dv=None, stream=None):
+    """attn_bwd for callers that cannot allocate device memory when they run the backward.
+
+    Same result as attn_bwd, but the float32 scratch comes from a fixed static array inside
+    the library (ATTN_BWD_NOALLOC_SCRATCH_BYTES, 32 MiB), so no workspace is passed and the
+    library allocates nothing.  Problems needing more scratch are refused with
+    ATTN_ERR_WORKSPACE.  Calls that overlap on the GPU share that array and race; the first
+    call on a device should come before any stream capture there.  Output tensors that are
+    not given are allocated here with PyTorch, so a caller that must not allocate passes
+    dq, dk and dv.
+    """
+    lib = load()
+    if getattr(lib.attn_bwd_noalloc, "argtypes", None) is None:
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.attn_bwd_noalloc.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp,
+                                         i32, vp, i64, i64, i32, vp, vp, vp, vp]
+        lib.attn_bwd_noalloc.restype = i32
+    B, H, n, d = _shape(q, k, v)
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(lib.attn_bwd_noalloc(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits),
+                                row_words, hs, int(kv_block), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _stream_ptr(stream)))
     return dq, dk, dv
 
 

@@ -91,6 +91,8 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
 
 }  // namespace
 
+void ea::set_last_error(const std::string& msg) { g_last_error = msg; }
+
 extern "C" {
 
 int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,

@@ -63,4 +63,7 @@ int launch_bwd_post(bool bf16, const AttnArgs& a, const float* acc, cudaStream_t
 size_t bwd_tc_workspace_bytes(int B, int H, int n, int d);
 size_t bwd_f32_workspace_bytes(int B, int H, int n, int d);
 
+// Sets the message attn_last_error() returns on the calling thread.
+void set_last_error(const std::string& msg);
+
 }  // namespace ea

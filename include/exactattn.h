@@ -116,6 +116,31 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c,
              void* stream);
 
 /*
+ * attn_bwd without a workspace argument, for callers that cannot allocate device memory at
+ * the time they call the backward: an engine or framework that owns every device allocation
+ * and gives its plugins no allocator, or a system that fixes its memory budget at start-up
+ * and allows no cudaMalloc afterwards.  The pages have no counterpart to this entry point; it
+ * computes exactly what attn_bwd computes.
+ *
+ * The float32 scratch (D and the dQ accumulator) lives in one static device array of
+ * ATTN_BWD_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU which loads this library holds
+ * until the process exits.  A problem with attn_bwd_workspace_bytes(...) larger than that
+ * is rejected with ATTN_ERR_WORKSPACE (see attn_last_error) before anything runs.  The first
+ * call on a device looks up the array's address on that device (cudaGetSymbolAddress); make
+ * it before any stream capture there.  All calls share the array, which keeps the last
+ * call's contents; each call rewrites and clears what it reads, but calls that overlap on the
+ * GPU (unordered streams) race on it.  No cudaMalloc, cudaFree or allocating library call is
+ * made.  Other arguments, outputs and errors as for attn_bwd.
+ */
+#define ATTN_BWD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int attn_bwd_noalloc(int dtype, int B, int H, int n, int d, float c,
+                     const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* d_o,
+                     int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                     int64_t mask_head_stride_words, int kv_block,
+                     void* dq, void* dk, void* dv, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the current device.
  * Returns ATTN_OK, ATTN_WARN_EMPTY_ROW, ATTN_ERR_DEVICE_TIMEOUT (a bounded wait inside a kernel
  * gave up; the kernel freed its resources and returned without finishing) or ATTN_ERR_CUDA.

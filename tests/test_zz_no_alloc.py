@@ -1,0 +1,75 @@
+"""attn_bwd_noalloc: the backward for callers that cannot allocate device memory.
+
+Engines that own every device allocation, or systems that freeze their memory budget at
+start-up, cannot hand the backward a freshly allocated workspace.  attn_bwd_noalloc takes its
+float32 scratch from a fixed static array in the library instead.  This file checks, through
+the C ABI, that it returns what attn_bwd returns (within the tolerances the other tests use)
+on two calls in a row, that it allocates no device memory, and that it refuses problems
+larger than its array.  It is collected last on purpose.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_gb300 as ea
+from synth import Workload
+
+from helpers import head_inputs, rel_frob_per_head, to_dev, tol_grad
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(lib):
+    f = lib.attn_bwd_noalloc
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    f.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, i32, vp, i64, i64, i32,
+                  vp, vp, vp, vp]
+    f.restype = i32
+    return f
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_noalloc_matches_attn_bwd_on_two_calls(dtype):
+    lib = ea.load()
+    noalloc = _noalloc(lib)
+    wl = Workload("noalloc", 21, 2, 3, 777, 64, dtype, "causal", 0.125)
+    inp = head_inputs(wl)
+    dev = {t: to_dev(inp[t], dtype) for t in inp}
+    q, k, v, g = dev["q"], dev["k"], dev["v"], dev["do"]
+    o, lse = ea.attn_fwd(q, k, v, wl.c, mask="causal")
+    ref = ea.attn_bwd(q, k, v, o, lse, g, wl.c, mask="causal")
+    code = ea.DTYPE_CODE[q.dtype]
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    outs = [tuple(torch.full_like(q, float("nan")) for _ in range(3)) for _ in range(2)]
+    torch.cuda.synchronize()
+    for call, (dq, dk, dv) in enumerate(outs):
+        free_before = torch.cuda.mem_get_info()[0]
+        rc = noalloc(code, wl.B, wl.H, wl.n, wl.d, wl.c, _p(q), _p(k), _p(v), _p(o), _p(lse),
+                     _p(g), 1, ctypes.c_void_p(0), 0, 0, 0, _p(dq), _p(dk), _p(dv), stream)
+        assert rc == 0, ea.attn_last_error()
+        assert ea.attn_device_status() == ea.ATTN_OK
+        if call == 1:  # the first call may load the library's module data on this device
+            assert torch.cuda.mem_get_info()[0] == free_before
+        for got, want in zip((dq, dk, dv), ref):
+            err = rel_frob_per_head(got, want.double().cpu().numpy())
+            assert torch.isfinite(got).all()
+            assert err.max() <= tol_grad(dtype)
+
+
+def test_noalloc_refuses_problems_larger_than_its_scratch():
+    lib = ea.load()
+    noalloc = _noalloc(lib)
+    need = lib.attn_bwd_workspace_bytes(2, 1, 64, 4096, 128)
+    assert need > (32 << 20)
+    buf = torch.empty(64, dtype=torch.bfloat16, device="cuda")
+    p = _p(buf)
+    rc = noalloc(2, 1, 64, 4096, 128, 0.1, p, p, p, p, p, p, 0, ctypes.c_void_p(0), 0, 0, 0,
+                 p, p, p, ctypes.c_void_p(0))
+    assert rc == ea.ATTN_ERR_WORKSPACE
+    assert "attn_bwd_noalloc" in ea.attn_last_error()
