@@ -1,0 +1,142 @@
+"""GPU vs oracle parity at the workloads' full sizes.
+
+Each workload runs at its full shape in the same launch configuration the library uses for
+the bench (one call over all heads).  Where the oracle cannot redo the whole problem in
+seconds, it recomputes sampled outputs one by one (sampled heads and query rows, always
+including the first and last rows of tiles and of the sequence), and properties that hold at
+any size are checked on every head (finite outputs, Σ_j dK_j = 0).
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_gb300 as ea
+from oracle import attention as ref
+from oracle import masks
+from synth import bitmap_mask, draw_head, pack_bitmap, workload
+
+from helpers import check_forward, check_grads, rel_frob_per_head, to_dev, tol_grad
+
+pytestmark = pytest.mark.gpu
+
+
+def _device_inputs(wl, tensors=("q", "k", "v")):
+    """Device tensors [B,H,n,d] built head by head from the seeded generator."""
+    out = {}
+    for t in tensors:
+        dev = torch.empty((wl.B, wl.H, wl.n, wl.d), dtype={"f32": torch.float32, "f16": torch.float16,
+                          "bf16": torch.bfloat16}[wl.dtype], device="cuda")
+        for bh in range(wl.heads):
+            dev[bh // wl.H, bh % wl.H] = to_dev(draw_head(wl, t, bh), wl.dtype)
+        out[t] = dev
+    return out
+
+
+def _sample_rows(n, rng, count=256):
+    fixed = [0, 1, 127, 128, 255, 256, n // 2, n - 2, n - 1]
+    rows = set(r for r in fixed if 0 <= r < n)
+    rows.update(rng.choice(n, size=min(count, n), replace=False).tolist())
+    return np.array(sorted(rows))
+
+
+def _check_rows(wl, o, lse, mk, heads, rows):
+    for bh in heads:
+        b, h = divmod(bh, wl.H)
+        q = draw_head(wl, "q", bh)[rows]
+        k, v = draw_head(wl, "k", bh), draw_head(wl, "v", bh)
+        y, l, _, _ = ref.forward_rows(q, k, v, wl.c, mk(bh, rows))
+        idx = torch.from_numpy(rows).cuda()
+        check_forward(o[b, h].index_select(0, idx), lse[b, h].index_select(0, idx), y, l, wl.dtype,
+                      f"{wl.name} head {bh}")
+
+
+def test_small_causal_f32_full():
+    wl = workload("small_causal_f32")
+    dev = _device_inputs(wl, ("q", "k", "v", "do"))
+    o, lse = ea.attn_fwd(dev["q"], dev["k"], dev["v"], wl.c, mask="causal", kv_block=wl.kv_block)
+    dq, dk, dv = ea.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], wl.c, mask="causal",
+                             kv_block=wl.kv_block)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    host = {t: dev[t].double().cpu().numpy() for t in dev}
+    mk = masks.causal(wl.n)
+    Y, L = ref.forward(host["q"], host["k"], host["v"], wl.c, mk)
+    check_forward(o, lse, Y, L, "f32", wl.name)
+    refs = ref.backward(host["q"], host["k"], host["v"], wl.c, mk, host["do"])
+    check_grads((dq, dk, dv), refs, "f32", wl.name)
+
+
+@pytest.mark.parametrize("name", ["overflow_f16_d16", "overflow_f16_d16_hot",
+                                  "overflow_f16_d64", "overflow_f16_d64_hot"])
+def test_overflow_workloads(name):
+    wl = workload(name)
+    dev = _device_inputs(wl)
+    o, lse = ea.attn_fwd(dev["q"], dev["k"], dev["v"], wl.c, mask="causal")
+    assert ea.attn_device_status() == ea.ATTN_OK
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(1)
+    _check_rows(wl, o, lse, masks.causal(wl.n), range(wl.heads), _sample_rows(wl.n, rng, 384))
+    if name.endswith("_hot"):
+        # the raw exponentials of these scores overflow fp16: the running maximum is needed
+        assert float(lse.max()) > np.log(65520.0)
+
+
+def test_training_workload_forward_and_backward():
+    wl = workload("train_bf16_d128")
+    dev = _device_inputs(wl, ("q", "k", "v", "do"))
+    ws = torch.empty(ea.attn_bwd_workspace_bytes(torch.bfloat16, wl.B, wl.H, wl.n, wl.d),
+                     dtype=torch.uint8, device="cuda")
+    o, lse = ea.attn_fwd(dev["q"], dev["k"], dev["v"], wl.c)
+    dq, dk, dv = ea.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], wl.c, workspace=ws)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+    # every head: the key gradients of a row sum to zero (Σ_j γ_ij = 0)
+    s = dk.float().sum(dim=2).norm(dim=-1) / dk.float().norm(dim=(2, 3))
+    assert float(s.max()) < 2e-2
+    rng = np.random.default_rng(3)
+    mk = masks.none(wl.n)
+    _check_rows(wl, o, lse, mk, [0, 37, 127], _sample_rows(wl.n, rng, 256))
+    for bh in (5, 122):
+        b, h = divmod(bh, wl.H)
+        q, k, v, g = (draw_head(wl, t, bh) for t in ("q", "k", "v", "do"))
+        rq, rk, rv, _, _ = ref.backward_head(q, k, v, wl.c, mk(bh, np.arange(wl.n)), g)
+        for name, got, want in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+            err = rel_frob_per_head(got[b, h], want[None])
+            assert err.max() <= tol_grad("bf16"), f"{name} head {bh}: {err.max():.3e}"
+
+
+@pytest.mark.parametrize("n", [16384, 65536])
+def test_long_context_causal_forward(n):
+    wl = workload(f"longctx_bf16_n{n}")
+    dev = _device_inputs(wl)
+    o, lse = ea.attn_fwd(dev["q"], dev["k"], dev["v"], wl.c, mask="causal")
+    assert ea.attn_device_status() == ea.ATTN_OK
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(4)
+    _check_rows(wl, o, lse, masks.causal(n), [0, 13, 31], _sample_rows(n, rng, 256))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_block_sparse_workload_every_key_block(dtype):
+    wl = workload(f"bitmap_{dtype}")
+    allowed = bitmap_mask(wl.n, wl.seed)
+    words = pack_bitmap(allowed)
+    bits = torch.from_numpy(words.view(np.int32)).cuda()
+    mk = masks.bitmap(words, wl.n)
+    dev = _device_inputs(wl, ("q", "k", "v", "do"))
+    host = {t: dev[t].double().cpu().numpy() for t in dev}
+    Y, L = ref.forward(host["q"], host["k"], host["v"], wl.c, mk)
+    refs = ref.backward(host["q"], host["k"], host["v"], wl.c, mk, host["do"])
+    outs = []
+    for b in wl.kv_blocks:
+        o, lse = ea.attn_fwd(dev["q"], dev["k"], dev["v"], wl.c, mask="bitmap", mask_bits=bits,
+                             kv_block=b)
+        dq, dk, dv = ea.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], wl.c,
+                                 mask="bitmap", mask_bits=bits, kv_block=b)
+        assert ea.attn_device_status() == ea.ATTN_OK
+        check_forward(o, lse, Y, L, dtype, f"{wl.name} b={b}")
+        check_grads((dq, dk, dv), refs, dtype, f"{wl.name} b={b}")
+        outs.append(o.double())
+    for o in outs[1:]:  # the key-block sizes agree with each other too
+        atol = 1e-5 if dtype == "f32" else 2 * (2e-2)
+        assert torch.all((o - outs[0]).abs() <= atol + (0 if dtype == "f32" else 4e-2) * outs[0].abs())
