@@ -73,18 +73,23 @@ struct Config {
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
   using TDQ = F32Tile<BQ, D>;  // float32 dQ block staged for the TMA reduce-add
-  // shared memory: K, V, two dSᵀ buffers, dQ staging, then NS stages of (Q, dO, LSE, D)
+  // Shared memory: K, V, NDS dSᵀ buffers, dQ staging, then NS stages of (Q, dO, LSE, D).
+  // A third Q/dO stage matters more than a second dSᵀ buffer: the load of block i+1 can then
+  // start when block i-2 releases its stage, a whole block earlier than with two stages.
   static constexpr int kBudget = 227 * 1024 - 2048;
-  static constexpr int kFixed = 2 * TK::kBytes + 2 * TS::kBytes + TDQ::kBytes;
   static constexpr int kStage = 2 * TQ::kBytes + 2 * BQ * 4;
-  static constexpr int kMaxStepBytes = 8 * 1024;
+  static constexpr int kMaxStepBytes = 4 * 1024;  // n <= 65536 at BQ = 64
+  static constexpr int kFixed1 = 2 * TK::kBytes + TS::kBytes + TDQ::kBytes;
+  static constexpr int kFit1 = (kBudget - kFixed1 - TS::kBytes - kMaxStepBytes) / kStage;
+  static constexpr int NDS = kFit1 >= 3 ? 2 : 1;
+  static constexpr int kFixed = kFixed1 + (NDS - 1) * TS::kBytes;
   static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes) / kStage;
   static constexpr int NS = kFit > 4 ? 4 : kFit;
-  static_assert(NS >= 2, "need two query stages");
+  static_assert(NS >= 3, "need three query stages");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + TK::kBytes;
   static constexpr int kOffDS = kOffV + TK::kBytes;
-  static constexpr int kOffDQ = kOffDS + 2 * TS::kBytes;
+  static constexpr int kOffDQ = kOffDS + NDS * TS::kBytes;
   static constexpr int kOffQ = kOffDQ + TDQ::kBytes;
   static constexpr int kOffG = kOffQ + NS * TQ::kBytes;
   static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [NS][BQ] LSE (log2 units)
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int BQ = C::BQ;
   constexpr int NS = C::NS;
   constexpr int NSB = C::NSB;
+  constexpr int NDS = C::NDS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -362,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars.dq_free, (i & 1) ^ 1, p.status, 26);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t dsb = smem_u32(sDS + (i & 1) * TS::kBytes);
+        const uint32_t dsb = smem_u32(sDS + (i % NDS) * TS::kBytes);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           if constexpr (C::kTr)
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kk > 0 ? 1u : 0u);
         }
         mma_commit(&bars.dq_full);
-        mma_commit(&bars.dss_free[i & 1]);
+        mma_commit(&bars.dss_free[i % NDS]);
       }
       mma_commit(&bars.kv_done);
     }
@@ -440,10 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.p_full[i % NSB]);
 
       ok = mbar_wait(&bars.dp_full, i & 1, p.status, 28);
-      if (ok && i >= 2) ok = mbar_wait(&bars.dss_free[i & 1], ((i >> 1) & 1) ^ 1, p.status, 29);
+      if (ok && i >= NDS)
+        ok = mbar_wait(&bars.dss_free[i % NDS], ((i / NDS) & 1) ^ 1, p.status, 29);
       if (!ok) break;
       tc_fence_after();
-      uint8_t* ds_tile = sDS + (i & 1) * TS::kBytes;
+      uint8_t* ds_tile = sDS + (i % NDS) * TS::kBytes;
 #pragma unroll
       for (int c0 = 0; c0 < BQ; c0 += 32) {
         uint32_t dp[32];
