@@ -330,14 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       s_phase ^= 1;
       tc_fence_after();
+      // All TMEM loads first, one wait: the row's BN raw scores land in registers.
       float sv[BN];
+      {
+        uint32_t rr[BN];
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tS + lane_off + c0, rr);
+        for (int c0 = 0; c0 < BN; c0 += 32)
+          tmem_ld32(tS + lane_off + c0, *reinterpret_cast<uint32_t(*)[32]>(rr + c0));
         tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 32; ++k) sv[c0 + k] = __uint_as_float(rr[k]) * sl2;
+        for (int k = 0; k < BN; ++k) sv[k] = __uint_as_float(rr[k]);
+      }
+      // With c > 0 the scale is folded into the exponent's FFMA and the maximum is taken on
+      // raw scores; otherwise (c <= 0) the scores are scaled first.
+      const bool fold = sl2 > 0.0f;
+      if (!fold) {
+#pragma unroll
+        for (int k = 0; k < BN; ++k) sv[k] *= sl2;
       }
       if (cls == kPartial) {
         if (p.mask_kind == kMaskCausal) {
@@ -359,16 +368,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (key0 + k >= n) sv[k] = -INFINITY;
         }
       }
-      float mx = sv[0];
+      // Row maximum with four independent accumulators (short dependency chains).
+      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-      for (int k = 1; k < BN; ++k) mx = fmaxf(mx, sv[k]);
+      for (int k = 0; k < BN; k += 8) {
+        a0 = fmax3(a0, sv[k], sv[k + 1]);
+        a1 = fmax3(a1, sv[k + 2], sv[k + 3]);
+        a2 = fmax3(a2, sv[k + 4], sv[k + 5]);
+        a3 = fmax3(a3, sv[k + 6], sv[k + 7]);
+      }
+      float mx = fmax3(a0, a1, fmaxf(a2, a3));
+      if (fold && mx != -INFINITY) mx *= sl2;
       float alpha = 1.0f;
       if (mx > m + kLazy || (m == -INFINITY && mx != -INFINITY)) {
         alpha = ex2(m - mx);  // m = -inf gives 0
         m = mx;
         l *= alpha;
       }
-      const float mu = (m == -INFINITY) ? 0.0f : m;
+      const float neg_mu = (m == -INFINITY) ? 0.0f : -m;
+      const float sc = fold ? sl2 : 1.0f;
       // z *= alpha: only after the first block, and only if some row of this warp needs it.
       if (!first && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll
@@ -382,19 +400,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       first = false;
-      float rowsum = 0.0f;
+      float r0 = 0.0f, r1 = 0.0f, r2 = 0.0f, r3 = 0.0f;
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2(sv[c0 + 2 * k] - mu);
-          const float p1 = ex2(sv[c0 + 2 * k + 1] - mu);
-          rowsum += p0 + p1;
+        for (int k = 0; k < 16; k += 2) {
+          const float p0 = ex2(fmaf(sv[c0 + 2 * k], sc, neg_mu));
+          const float p1 = ex2(fmaf(sv[c0 + 2 * k + 1], sc, neg_mu));
+          const float p2 = ex2(fmaf(sv[c0 + 2 * k + 2], sc, neg_mu));
+          const float p3 = ex2(fmaf(sv[c0 + 2 * k + 3], sc, neg_mu));
+          r0 += p0;
+          r1 += p1;
+          r2 += p2;
+          r3 += p3;
           pk[k] = pack2<kBf16>(p0, p1);
+          pk[k + 1] = pack2<kBf16>(p2, p3);
         }
         tmem_st16(tS + lane_off + c0 / 2, pk);
       }
+      const float rowsum = (r0 + r1) + (r2 + r3);
       l += rowsum;
       tmem_wait_st();
       tc_fence_before();

@@ -267,6 +267,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Pack two floats into one 32-bit word of 16-bit values: `lo` in bits 0-15, `hi` in 16-31.
 template <bool kBf16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
