@@ -21,6 +21,7 @@ __all__ = [
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
     "attn_device_status", "attn_last_error", "attention", "attn_bwd_noalloc",
+    "attn_selftest_wait_timeout",
 ]
 
 ATTN_OK = 0
@@ -184,6 +185,14 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, c, mask="none", mask_bits=None,
                                 row_words, hs, int(kv_block), _ptr(dq), _ptr(dk), _ptr(dv),
                                 _stream_ptr(stream)))
     return dq, dk, dv
+
+
+def attn_selftest_wait_timeout(stream=None) -> int:
+    """Launch the library's failure-path self-test (a bounded wait that must time out)."""
+    lib = load()
+    lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
+    lib.attn_selftest_wait_timeout.restype = ctypes.c_int
+    return _check(lib.attn_selftest_wait_timeout(_stream_ptr(stream)))
 
 
 def attn_device_status(stream=None) -> int:

@@ -8,6 +8,7 @@
 
 #include "exactattn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -87,6 +88,17 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.mask_head_stride_words = head_stride;
   a.kv_block = kv_block;
   return a;
+}
+
+// One warp waits, with the library's bounded wait, on an mbarrier that nothing arrives on.
+__global__ void selftest_wait_kernel(uint32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    ea::mbar_init(&bar, 1);
+    ea::fence_barrier_init();
+  }
+  __syncwarp();
+  ea::mbar_wait(&bar, 0, status, 0x3F);
 }
 
 }  // namespace
@@ -178,6 +190,16 @@ int attn_device_status(void* stream) {
     return fail(ATTN_ERR_DEVICE_TIMEOUT, buf);
   }
   if (word & 2u) return ATTN_WARN_EMPTY_ROW;
+  return ATTN_OK;
+}
+
+int attn_selftest_wait_timeout(void* stream) {
+  uint32_t* st = nullptr;
+  if (int rc = status_ptr(&st)) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, std::string("self-test launch: ") + cudaGetErrorString(e));
   return ATTN_OK;
 }
 

@@ -147,6 +147,15 @@ int attn_bwd_noalloc(int dtype, int B, int H, int n, int d, float c,
  */
 int attn_device_status(void* stream);
 
+/*
+ * Self-test of the failure path (no counterpart on the pages): launches one warp that waits,
+ * with the same bounded wait every kernel of the library uses, on a barrier nothing ever
+ * completes.  After the wait's limit (2 s) the kernel records a timeout in the device status
+ * word and returns, so the next attn_device_status(stream) returns ATTN_ERR_DEVICE_TIMEOUT
+ * and the CUDA context stays usable.  Asynchronous on `stream`.
+ */
+int attn_selftest_wait_timeout(void* stream);
+
 /* Message describing the calling thread's most recent failed call ("" if none). */
 const char* attn_last_error(void);
 
