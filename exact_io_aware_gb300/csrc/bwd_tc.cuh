@@ -77,6 +77,8 @@ struct Config {
   // A third Q/dO stage matters more than a second dSᵀ buffer: the load of block i+1 can then
   // start when block i-2 releases its stage, a whole block earlier than with two stages.
   static constexpr int kBudget = 227 * 1024 - 2048;
+  // per stage: Q, dO, LSE, D (bitmap masks add the block's allowed-key words after the step
+  // table, sized per launch)
   static constexpr int kStage = 2 * TQ::kBytes + 2 * BQ * 4;
   static constexpr int kMaxStepBytes = 4 * 1024;  // n <= 65536 at BQ = 64
   static constexpr int kFixed1 = 2 * TK::kBytes + TS::kBytes + TDQ::kBytes;
@@ -95,9 +97,12 @@ struct Config {
   static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [NS][BQ] LSE (log2 units)
   static constexpr int kOffD = kOffL + NS * BQ * 4;      // [NS][BQ] D
   static constexpr int kOffSteps = kOffD + NS * BQ * 4;
-  static size_t smem_bytes(int n) {
-    const int nqb = (n + BQ - 1) / BQ;
-    return 1024 + kOffSteps + 4 * static_cast<size_t>(nqb);
+  // [NS][BQ][4] mask words, after the step table (bitmap masks only)
+  __host__ __device__ static constexpr int off_bits(int n) {
+    return (kOffSteps + 4 * ((n + BQ - 1) / BQ) + 15) / 16 * 16;
+  }
+  static size_t smem_bytes(int n, bool bitmap) {
+    return 1024 + static_cast<size_t>(off_bits(n)) + (bitmap ? NS * BQ * 16 : 0);
   }
 };
 
@@ -160,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sG = smem + C::kOffG;
   float* sL = reinterpret_cast<float*>(smem + C::kOffL);
   float* sD = reinterpret_cast<float*>(smem + C::kOffD);
+  uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + C::off_bits(p.n));
   uint32_t* steps = reinterpret_cast<uint32_t*>(smem + C::kOffSteps);
   __shared__ Barriers bars;
 
@@ -292,6 +298,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         sL[s * BQ + t] = lv == -INFINITY ? INFINITY : lv * 1.4426950408889634f;
         sD[s * BQ + t] = q < n ? __ldg(d_h + q) : 0.0f;
       }
+      if (p.mask_kind == kMaskBitmap && ((steps[i] >> 16) & 3u) == kPartial) {
+        // words of allowed-key bits for rows q0.. of this block and keys key0..key0+127;
+        // rows past n and keys past n read as not allowed
+        const uint32_t* bits = p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words;
+        for (int e = lane; e < BQ * 4; e += 32) {
+          const int t = e >> 2, w = e & 3;
+          const int q = q0 + t, kw = key0 + 32 * w;
+          uint32_t word = 0u;
+          if (q < n && kw < n) {
+            word = __ldg(bits + static_cast<int64_t>(q) * p.mask_row_words + kw / 32);
+            const int nk = n - kw;
+            if (nk < 32) word &= (1u << nk) - 1u;
+          }
+          sBits[(s * BQ + t) * 4 + w] = word;
+        }
+      }
       mbar_arrive(&bars.ld_full[s]);
     }
   } else if (warp == kMmaWarp) {
@@ -389,10 +411,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = key0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = p.c * 1.4426950408889634f;
-    const uint32_t* bits_base =
-        p.mask_kind == kMaskBitmap
-            ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words + (j < n ? j : 0) / 32
-            : nullptr;
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
@@ -418,14 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stays one compact run of instructions.
         if (partial) {
           if (p.mask_kind == kMaskBitmap) {
+            // this warp's 32 keys share one word per query row (staged by the producer)
+            const uint32_t* wb = sBits + ((i % NS) * BQ + c0) * 4 + warp;
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int q = q0 + c0 + k;
-              const bool allowed =
-                  q < n && j < n &&
-                  ((__ldg(bits_base + static_cast<int64_t>(q) * p.mask_row_words) >> (j & 31)) & 1u);
-              if (!allowed) pv[k] = 0.0f;
-            }
+            for (int k = 0; k < 32; ++k)
+              if (!((wb[4 * k] >> lane) & 1u)) pv[k] = 0.0f;
           } else {
             const bool causal = p.mask_kind == kMaskCausal;
 #pragma unroll

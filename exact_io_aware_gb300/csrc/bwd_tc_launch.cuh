@@ -11,7 +11,7 @@ constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 template <bool kBf16, int D>
 int run(const AttnArgs& a, float* Dv, float* acc, cudaStream_t s, std::string& err) {
   using Cfg = Config<D>;
-  const size_t smem = Cfg::smem_bytes(a.n);
+  const size_t smem = Cfg::smem_bytes(a.n, a.mask_kind == kMaskBitmap);
   if (smem > static_cast<size_t>(kMaxDynSmem)) {
     err = "n too large for the backward step table";
     return -2;

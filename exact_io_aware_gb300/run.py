@@ -1,16 +1,20 @@
-"""Run the attention forward/backward on a synthetic problem a few times.
+"""Run the attention forward/backward on a synthetic problem and time it.
 
-Meant for profilers (ncu) and quick timing of one shape:
+For profilers (ncu) and for timing one shape or one named workload:
 
-    python -m exact_io_aware_gb300.run --B 1 --H 64 --n 4096 --d 128 --dtype bf16 \\
-        --mask none --iters 2
+    python -m exact_io_aware_gb300.run --B 1 --H 64 --n 4096 --d 128 --iters 2
+    python -m exact_io_aware_gb300.run --workload longctx_bf16_n65536 --iters 5
 
-Inputs are seeded N(0,1) tensors generated on the device.  Prints the device time of the
-last forward and backward call.
+Inputs are seeded N(0,1) tensors generated on the device (the workload's query scale
+applied); a bitmap workload uses the seeded allowed-key sets of ``synth``.  Prints the mean
+CUDA-event time of the forward and backward calls after one untimed call, with TFLOP/s
+counted the standard way (forward 4·B·H·n²·d·κ, backward 2.5 times that; κ = 1/2 causal,
+popcount/n² for a bitmap).
 """
 from __future__ import annotations
 
 import argparse
+import json
 import os
 import sys
 
@@ -20,11 +24,13 @@ if ROOT not in sys.path:
 
 
 def main(argv=None):
+    import numpy as np
     import torch
 
     import exact_io_aware_gb300 as ea
 
     ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default=None, help="named workload from synth.CONFIGS")
     ap.add_argument("--B", type=int, default=1)
     ap.add_argument("--H", type=int, default=64)
     ap.add_argument("--n", type=int, default=4096)
@@ -34,29 +40,61 @@ def main(argv=None):
     ap.add_argument("--kv-block", type=int, default=0)
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
-    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[a.dtype]
+
+    B, H, n, d, dtype, mask, kvb, qs = a.B, a.H, a.n, a.d, a.dtype, a.mask, a.kv_block, 1.0
+    c = d ** -0.5
+    bits = None
+    kappa = 0.5 if mask == "causal" else 1.0
+    fwd_only = a.fwd_only
+    name = "custom"
+    if a.workload:
+        from synth import bitmap_mask, pack_bitmap, workload
+        wl = workload(a.workload)
+        B, H, n, d, dtype, mask, c, qs = wl.B, wl.H, wl.n, wl.d, wl.dtype, wl.mask, wl.c, wl.q_scale
+        kvb = a.kv_block or wl.kv_block
+        fwd_only = fwd_only or "bwd" not in wl.passes
+        name = wl.name
+        kappa = 0.5 if mask == "causal" else 1.0
+        if mask == "bitmap":
+            allowed = bitmap_mask(n, wl.seed)
+            kappa = float(allowed.mean())
+            bits = torch.from_numpy(pack_bitmap(allowed).view(np.int32)).cuda()
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dtype]
     ea.load()
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
-    shape = (a.B, a.H, a.n, a.d)
-    q, k, v, do = (torch.randn(shape, device="cuda", generator=g).to(dt) for _ in range(4))
-    c = a.d ** -0.5
+    shape = (B, H, n, d)
+    q, k, v, do = (torch.randn(shape, device="cuda", generator=g) for _ in range(4))
+    q = (q * qs).to(dt)
+    k, v, do = k.to(dt), v.to(dt), do.to(dt)
     o = torch.empty_like(q)
     lse = torch.empty(shape[:3], device="cuda", dtype=torch.float32)
     ws = torch.empty(ea.attn_bwd_workspace_bytes(dt, *shape), dtype=torch.uint8, device="cuda")
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    for _ in range(a.iters):
-        ev[0].record()
-        ea.attn_fwd(q, k, v, c, mask=a.mask, kv_block=a.kv_block, o=o, lse=lse)
-        ev[1].record()
-        if not a.fwd_only:
-            ea.attn_bwd(q, k, v, o, lse, do, c, mask=a.mask, kv_block=a.kv_block, workspace=ws)
-        ev[2].record()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.iters + 1)]
+    for e in ev:
+        e[0].record()
+        ea.attn_fwd(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse)
+        e[1].record()
+        if not fwd_only:
+            ea.attn_bwd(q, k, v, o, lse, do, c, mask=mask, mask_bits=bits, kv_block=kvb,
+                        workspace=ws)
+        e[2].record()
     torch.cuda.synchronize()
     status = ea.attn_device_status()
-    print(f"fwd {ev[0].elapsed_time(ev[1]):.3f} ms  bwd {ev[1].elapsed_time(ev[2]):.3f} ms  "
-          f"status {status}")
+    fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
+    bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev[1:]])) if not fwd_only else None
+    fl = 4.0 * B * H * n * n * d * kappa
+    out = {"workload": name, "B": B, "H": H, "n": n, "d": d, "dtype": dtype, "mask": mask,
+           "kv_block": kvb, "kappa": kappa, "fwd_ms": fwd_ms,
+           "fwd_tflops": fl / (fwd_ms / 1e3) / 1e12, "status": status}
+    if bwd_ms is not None:
+        out.update(bwd_ms=bwd_ms, bwd_tflops=2.5 * fl / (bwd_ms / 1e3) / 1e12)
+    if a.json:
+        print(json.dumps(out))
+    else:
+        print(" ".join(f"{k}={v:.4g}" if isinstance(v, float) else f"{k}={v}" for k, v in out.items()))
     return 0 if status == ea.ATTN_OK else 1
 
 
