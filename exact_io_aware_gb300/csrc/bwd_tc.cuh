@@ -17,9 +17,11 @@
 //   dQ  = dS K   (d <= 64)  or  dQᵀ = Kᵀ dSᵀ (d = 128, so the 128-lane accumulator holds d)
 // and dQ is added into a float32 accumulator in global memory; dK and dV stay in tensor memory
 // until the last block.  Roles:
-//   warps 0-3  softmax (P and dS)            warps 4-7  dQ reduction and dK/dV epilogue
-//   warp  8    TMA producer (K, V once; Q, dO per block through an NS-stage ring)
-//   warp  9    TMEM allocator and MMA issuer
+//   warps 0-7  softmax (P and dS): warp w owns TMEM lanes 32 (w % 4).. and half w / 4 of the
+//              block's query columns (P and dS are elementwise, so the halves never meet)
+//   warps 8-11 dQ reduction and dK/dV epilogue
+//   warp  12   TMA producer (K, V once; Q, dO per block through an NS-stage ring)
+//   warp  13   TMEM allocator and MMA issuer
 // With d = 128 a block has 64 queries and two S buffers, so S of the next block is computed
 // while the softmax warps still work on the current one.
 #pragma once
@@ -33,9 +35,11 @@ namespace ea {
 namespace bwd {
 
 constexpr int kKeys = 128;
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 448;
+constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each on half the block's queries
+constexpr int kReduceWarp0 = 8;   // warps 8-11: dQ reduction and the dK/dV epilogue
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
 
 struct BwdParams {
@@ -126,6 +130,14 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Column (within an S or dP buffer) of the 16-bit pair holding query column c.  Each half of
+// the block's queries packs its pairs at the start of its own fp32 column range, so the two
+// softmax warps sharing a lane quadrant never overwrite columns the other still reads.
+template <int BQ>
+__host__ __device__ constexpr int packed_col(int c) {
+  return (c / (BQ / 2)) * (BQ / 2) + (c % (BQ / 2)) / 2;
+}
+
 template <bool kBf16>
 __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   if constexpr (kBf16) {
@@ -191,10 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.dss_free[b], 1);
-      mbar_init(&bars.p_full[b], 4);
+      mbar_init(&bars.p_full[b], kSoftmaxWarps);
     }
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.ds_full, 4);
+    mbar_init(&bars.ds_full, kSoftmaxWarps);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 4);
     mbar_init(&bars.kv_done, 1);
@@ -368,14 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + (i % NSB) * BQ + kk * 8, TQ::desc_mn(gb, kk),
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + (i % NSB) * BQ + packed_col<BQ>(16 * kk),
+                 TQ::desc_mn(gb, kk),
                  id_kv, (i > 0 || kk > 0) ? 1u : 0u);
         ok = mbar_wait(&bars.ds_full, i & 1, p.status, 25);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + kk * 8, TQ::desc_mn(qb, kk), id_kv,
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col<BQ>(16 * kk), TQ::desc_mn(qb, kk),
+                 id_kv,
                  (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.qdo_empty[s]);
         if (i + 1 < nsteps) {
@@ -405,11 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit(&bars.kv_done);
     }
-  } else if (warp < 4) {
+  } else if (warp < kSoftmaxWarps) {
     // ---------------------------------------------------------------- softmax: P and dS
-    const int r = tid;  // key row within the tile = TMEM lane
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;  // key row within the tile = TMEM lane
     const int j = key0 + r;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    constexpr int kHalf = BQ / 2;  // query columns of this warp: [c_lo, c_lo + kHalf)
+    const int c_lo = (warp / 4) * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
@@ -425,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tS = tmem + C::kColS + (i % NSB) * BQ + lane_off;
       const uint32_t tP = tmem + C::kColDP + lane_off;
 #pragma unroll
-      for (int c0 = 0; c0 < BQ; c0 += 32) {
+      for (int cc = 0; cc < kHalf; cc += 32) {
+        const int c0 = c_lo + cc;
         uint32_t rr[32];
         tmem_ld32(tS + c0, rr);
         tmem_wait_ld();
@@ -437,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (partial) {
           if (p.mask_kind == kMaskBitmap) {
             // this warp's 32 keys share one word per query row (staged by the producer)
-            const uint32_t* wb = sBits + ((i % NS) * BQ + c0) * 4 + warp;
+            const uint32_t* wb = sBits + ((i % NS) * BQ + c0) * 4 + quad;
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               if (!((wb[4 * k] >> lane) & 1u)) pv[k] = 0.0f;
@@ -453,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) pk[k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
-        tmem_st16(tS + c0 / 2, pk);
+        tmem_st16(tS + packed_col<BQ>(c0), pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -467,11 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint8_t* ds_tile = sDS + (i % NDS) * TS::kBytes;
 #pragma unroll
-      for (int c0 = 0; c0 < BQ; c0 += 32) {
+      for (int cc = 0; cc < kHalf; cc += 32) {
+        const int c0 = c_lo + cc;
         uint32_t dp[32];
         uint32_t pp[16];
         tmem_ld32(tP + c0, dp);
-        tmem_ld16(tS + c0 / 2, pp);
+        tmem_ld16(tS + packed_col<BQ>(c0), pp);
         tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
@@ -482,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float g1 = p1 * (__uint_as_float(dp[2 * k + 1]) - Dd[c0 + 2 * k + 1]);
           pk[k] = pack2<kBf16>(g0, g1);
         }
-        tmem_st16(tP + c0 / 2, pk);
+        tmem_st16(tP + packed_col<BQ>(c0), pk);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           *reinterpret_cast<uint4*>(ds_tile + TS::offset(r, c0 + 8 * u)) =
@@ -496,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- dQ reduction, epilogue
-    const int quad = warp - 4;
+    const int quad = warp - kReduceWarp0;
     const int r = quad * 32 + lane;  // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     // Each block's dQ leaves tensor memory through a swizzled float32 staging tile and one
