@@ -65,12 +65,15 @@ struct Config {
   using TQ = Tile<BQ, D>;      // Q, dO stages
   using TS = Tile<kKeys, BQ>;  // dSᵀ: rows = keys, cols = queries
   static constexpr int kDqCols = pad32(kTr ? BQ : D);
-  static constexpr int kTwoS = 2 * BQ + BQ + kDqCols + 2 * pad32(D);
-  static constexpr int NSB = kTwoS <= 512 ? 2 : 1;
+  // One S buffer (P stays in the softmax warps' registers between its two passes, so S is free
+  // once dV has read P) and, where tensor memory allows, two dP buffers so dP of the next block
+  // is computed while the softmax warps still work on this one.
+  static constexpr int kTwoDP = BQ + 2 * BQ + kDqCols + 2 * pad32(D);
+  static constexpr int NDP = kTwoDP <= 512 ? 2 : 1;
   // tensor-memory columns
-  static constexpr int kColS = 0;  // S buffer b at b * BQ
-  static constexpr int kColDP = NSB * BQ;
-  static constexpr int kColDV = kColDP + BQ;
+  static constexpr int kColS = 0;
+  static constexpr int kColDP = BQ;  // dP buffer b at kColDP + b * BQ
+  static constexpr int kColDV = kColDP + NDP * BQ;
   static constexpr int kColDK = kColDV + pad32(D);
   static constexpr int kColDQ = kColDK + pad32(D);
   static constexpr int kTmemCols = kColDQ + kDqCols;
@@ -113,8 +116,8 @@ struct Config {
 struct Barriers {
   uint64_t kv_full;
   uint64_t qdo_full[4], qdo_empty[4], ld_full[4];
-  uint64_t s_full[2];
-  uint64_t p_full[2], dp_full, ds_full;
+  uint64_t s_full;
+  uint64_t p_full, dp_full[2], ds_full[2];
   uint64_t dss_free[2];
   uint64_t dq_full, dq_free;
   uint64_t kv_done;
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TDQ = typename C::TDQ;
   constexpr int BQ = C::BQ;
   constexpr int NS = C::NS;
-  constexpr int NSB = C::NSB;
+  constexpr int NDP = C::NDP;
   constexpr int NDS = C::NDS;
 
   extern __shared__ uint8_t smem_raw[];
@@ -197,16 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.qdo_empty[s], 1);
       mbar_init(&bars.ld_full[s], 32);
     }
-    // p_full is per S buffer: with two buffers a fast softmax warp may publish P of the next
-    // block before a slow warp has published P of this one, and one shared barrier would then
-    // count that early arrival towards the wrong phase.
+    // ds_full is per dP buffer: dP of the next block is issued before this block's dS is
+    // published, so a fast softmax warp may publish dS of the next block before a slow warp has
+    // published this one, and a single barrier would count that arrival towards the wrong phase.
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, kSoftmaxWarps);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.dss_free[b], 1);
-      mbar_init(&bars.p_full[b], kSoftmaxWarps);
+      mbar_init(&bars.dp_full[b], 1);
+      mbar_init(&bars.ds_full[b], kSoftmaxWarps);
     }
-    mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.ds_full, kSoftmaxWarps);
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.dq_free, 4);
     mbar_init(&bars.kv_done, 1);
@@ -344,16 +347,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qb = smem_u32(sQ + (i % NS) * TQ::kBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS + (i % NSB) * BQ, TK::desc_k(sk, kk), TQ::desc_k(qb, kk), id_s,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(&bars.s_full[i % NSB]);
+          mma_ss(tmem + C::kColS, TK::desc_k(sk, kk), TQ::desc_k(qb, kk), id_s, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.s_full);
       };
       auto issue_dp = [&](int i) {
         const uint32_t gb = smem_u32(sG + (i % NS) * TQ::kBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, TK::desc_k(sv, kk), TQ::desc_k(gb, kk), id_s, kk > 0 ? 1u : 0u);
-        mma_commit(&bars.dp_full);
+          mma_ss(tmem + C::kColDP + (i % NDP) * BQ, TK::desc_k(sv, kk), TQ::desc_k(gb, kk), id_s,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&bars.dp_full[i % NDP]);
       };
       if (ok && nsteps > 0) {
         ok = wait_qdo(0);
@@ -363,44 +366,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_dp(0);
         }
       }
-      // Order per block i: [S_{i+1}], dV_i, dK_i, [S_{i+1}], dP_{i+1}, dQ_i.  dP_{i+1} goes
-      // before dQ_i so the softmax warps can start dS_{i+1} while dQ_i is reduced.
+      // Order per block i: [dP_{i+1}], dV_i, S_{i+1}, dK_i, [dP_{i+1}], dQ_i.  With two dP
+      // buffers dP_{i+1} goes first, so the softmax warps find it ready when they finish dS_i;
+      // S_{i+1} follows dV_i, the last reader of P_i in the (single) S buffer.
       for (int i = 0; i < nsteps && ok; ++i) {
         const int s = i % NS;
         const uint32_t qb = smem_u32(sQ + s * TQ::kBytes);
         const uint32_t gb = smem_u32(sG + s * TQ::kBytes);
-        if (NSB == 2 && i + 1 < nsteps) {
+        if (NDP == 2 && i + 1 < nsteps) {
           ok = wait_qdo(i + 1);
           if (!ok) break;
           tc_fence_after();
-          issue_s(i + 1);
+          issue_dp(i + 1);
         }
-        ok = mbar_wait(&bars.p_full[i % NSB], (i / NSB) & 1, p.status, 24);
+        ok = mbar_wait(&bars.p_full, i & 1, p.status, 24);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + (i % NSB) * BQ + packed_col<BQ>(16 * kk),
-                 TQ::desc_mn(gb, kk),
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col<BQ>(16 * kk), TQ::desc_mn(gb, kk),
                  id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        ok = mbar_wait(&bars.ds_full, i & 1, p.status, 25);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col<BQ>(16 * kk), TQ::desc_mn(qb, kk),
-                 id_kv,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.qdo_empty[s]);
         if (i + 1 < nsteps) {
-          if (NSB == 1) {
+          if (NDP == 1) {
             ok = wait_qdo(i + 1);
             if (!ok) break;
             tc_fence_after();
-            issue_s(i + 1);
           }
-          issue_dp(i + 1);
+          issue_s(i + 1);
         }
+        ok = mbar_wait(&bars.ds_full[i % NDP], (i / NDP) & 1, p.status, 25);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + (i % NDP) * BQ + packed_col<BQ>(16 * kk),
+                 TQ::desc_mn(qb, kk), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.qdo_empty[s]);
+        if (NDP == 1 && i + 1 < nsteps) issue_dp(i + 1);
         ok = mbar_wait(&bars.dq_free, (i & 1) ^ 1, p.status, 26);
         if (!ok) break;
         tc_fence_after();
@@ -436,11 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* Dd = sD + (i % NS) * BQ;
       ok = mbar_wait(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
       if (!ok) break;
-      ok = mbar_wait(&bars.s_full[i % NSB], (i / NSB) & 1, p.status, 27);
+      ok = mbar_wait(&bars.s_full, i & 1, p.status, 27);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem + C::kColS + (i % NSB) * BQ + lane_off;
-      const uint32_t tP = tmem + C::kColDP + lane_off;
+      const uint32_t tS = tmem + C::kColS + lane_off;
+      const uint32_t tP = tmem + C::kColDP + (i % NDP) * BQ + lane_off;
+      uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
@@ -470,15 +473,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
+        for (int k = 0; k < 16; ++k) {
+          pk[k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
+          pkeep[cc / 2 + k] = pk[k];
+        }
         tmem_st16(tS + packed_col<BQ>(c0), pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full[i % NSB]);
+      if (lane == 0) mbar_arrive(&bars.p_full);
 
-      ok = mbar_wait(&bars.dp_full, i & 1, p.status, 28);
+      ok = mbar_wait(&bars.dp_full[i % NDP], (i / NDP) & 1, p.status, 28);
       if (ok && i >= NDS)
         ok = mbar_wait(&bars.dss_free[i % NDS], ((i / NDS) & 1) ^ 1, p.status, 29);
       if (!ok) break;
@@ -488,10 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
         uint32_t dp[32];
-        uint32_t pp[16];
         tmem_ld32(tP + c0, dp);
-        tmem_ld16(tS + packed_col<BQ>(c0), pp);
         tmem_wait_ld();
+        const uint32_t* pp = pkeep + cc / 2;
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -511,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.ds_full);
+      if (lane == 0) mbar_arrive(&bars.ds_full[i % NDP]);
     }
   } else {
     // ---------------------------------------------------------------- dQ reduction, epilogue
