@@ -3,8 +3,9 @@
 // Preprocessing computes the per-row term of the reverse procedure of "Exact tiled attention
 // and memory-aware differentiation", delta_i = sum_a G_ia Y_ia, from the stored output O and
 // the upstream dO (the "D vector" that "Bellek Duvarının Fiziği" notes comes for free from
-// O).  It can also clear the float32 dQ accumulator of the tensor-core backward.
-// Postprocessing scales that accumulator by c and rounds it to the 16-bit output type.
+// O).  For the tensor-core backward it writes a padded per-row table (LSE in log2 units and D)
+// that the kernels copy into shared memory in 512-byte bulk transfers.  Postprocessing scales a
+// float32 dQ accumulator by c and rounds it to the 16-bit output type.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -43,6 +44,56 @@ __global__ void __launch_bounds__(256) pre_kernel(const T* __restrict__ O, const
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t e = tid; e < zero_vec4; e += nth) zero[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Row table of the tensor-core backward, padded to n_pad rows per head: L2 = LSE * log2(e)
+// (+inf for rows with no allowed key and rows past n, so that their probabilities are 0) and
+// D = rowsum(dO * O) (0 past n).  d/4 lanes cover a row with 8-byte loads (4 elements), so a
+// warp takes 32/(d/4) rows at once.
+template <typename T>
+__global__ void __launch_bounds__(256) pre_rows_kernel(const T* __restrict__ O,
+                                                       const T* __restrict__ G,
+                                                       const float* __restrict__ lse,
+                                                       float* __restrict__ L2,
+                                                       float* __restrict__ Dv, int64_t heads, int n,
+                                                       int n_pad, int d) {
+  const int lpr = d / 4;
+  const int rpw = 32 / lpr;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / lpr, part = lane % lpr;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t total = heads * n_pad;
+  for (int64_t base = warp0 * rpw; base < total; base += nwarps * rpw) {
+    const int64_t rr = base + sub;
+    int64_t bh = 0, r = 0;
+    bool live = false;
+    if (rr < total) {
+      bh = rr / n_pad;
+      r = rr - bh * n_pad;
+      live = r < n;
+    }
+    float acc = 0.0f;
+    if (live) {
+      const int64_t off = (bh * n + r) * d + 4 * part;
+      const uint2 ov = *reinterpret_cast<const uint2*>(O + off);
+      const uint2 gv = *reinterpret_cast<const uint2*>(G + off);
+      const T* o4 = reinterpret_cast<const T*>(&ov);
+      const T* g4 = reinterpret_cast<const T*>(&gv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc = fmaf(to_f(o4[e]), to_f(g4[e]), acc);
+    }
+    for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    if (rr < total && part == 0) {
+      float l2 = INFINITY;
+      if (live) {
+        const float lv = lse[bh * n + r];
+        if (lv != -INFINITY) l2 = lv * 1.4426950408889634f;
+      }
+      L2[rr] = l2;
+      Dv[rr] = live ? acc : 0.0f;
+    }
   }
 }
 
@@ -98,6 +149,27 @@ int launch_bwd_pre(int dtype, const AttnArgs& a, float* D, float* zero, size_t z
           a.d, z, zv);
       break;
   }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    err = std::string("backward preprocessing launch: ") + cudaGetErrorString(e);
+    return -5;
+  }
+  return 0;
+}
+
+int launch_bwd_pre_rows(bool bf16, const AttnArgs& a, float* L2, float* Dv, int n_pad,
+                        cudaStream_t s, std::string& err) {
+  const int64_t heads = static_cast<int64_t>(a.B) * a.H;
+  const int rpw = 32 / (a.d / 4);
+  const int grid = aux::grid_for(heads * n_pad, 8 * rpw);
+  if (bf16)
+    aux::pre_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.d_o), a.lse, L2,
+        Dv, heads, a.n, n_pad, a.d);
+  else
+    aux::pre_rows_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(a.o),
+                                                      static_cast<const __half*>(a.d_o), a.lse, L2,
+                                                      Dv, heads, a.n, n_pad, a.d);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("backward preprocessing launch: ") + cudaGetErrorString(e);

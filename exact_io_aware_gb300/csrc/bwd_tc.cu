@@ -1,37 +1,31 @@
-// tcgen05 backward: preprocessing (D and a cleared dQ accumulator), the main kernel, and the
-// dQ postprocessing, all on the caller's stream.
+// tcgen05 backward: D = rowsum(dO * O), then the dK/dV kernel (key tiles) and the dQ kernel
+// (query tiles), all on the caller's stream.
 #include "kernels.h"
 
 namespace ea {
-int launch_bwd_tc_d16(bool, const AttnArgs&, float*, float*, cudaStream_t, std::string&);
-int launch_bwd_tc_d32(bool, const AttnArgs&, float*, float*, cudaStream_t, std::string&);
-int launch_bwd_tc_d64(bool, const AttnArgs&, float*, float*, cudaStream_t, std::string&);
-int launch_bwd_tc_d128(bool, const AttnArgs&, float*, float*, cudaStream_t, std::string&);
+int launch_bwd_tc_d16(bool, const AttnArgs&, const float*, cudaStream_t, std::string&);
+int launch_bwd_tc_d32(bool, const AttnArgs&, const float*, cudaStream_t, std::string&);
+int launch_bwd_tc_d64(bool, const AttnArgs&, const float*, cudaStream_t, std::string&);
+int launch_bwd_tc_d128(bool, const AttnArgs&, const float*, cudaStream_t, std::string&);
 
-namespace {
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-}  // namespace
-
-// Workspace: D [B*H*n] float32, then the dQ accumulator [B*H*n*d] float32.
-size_t bwd_tc_workspace_bytes(int B, int H, int n, int d) {
-  const size_t rows = static_cast<size_t>(B) * H * n;
-  return align256(rows * 4) + align256(rows * d * 4);
+// Workspace: the row table, L2 then D, each [B*H][n_pad] float32 with n_pad = n rounded up to
+// 128 (so every 128-row block of it is a whole, 512-byte-aligned bulk copy).
+size_t bwd_tc_workspace_bytes(int B, int H, int n, int) {
+  const size_t rows = static_cast<size_t>(B) * H * bwd_pad_rows(n);
+  return 2 * rows * 4;
 }
 
 int launch_bwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
-  const size_t rows = static_cast<size_t>(a.B) * a.H * a.n;
-  float* Dv = static_cast<float*>(a.workspace);
-  float* acc = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + align256(rows * 4));
-  if (int rc = launch_bwd_pre(bf16 ? 2 : 1, a, Dv, acc, rows * a.d, s, err)) return rc;
-  int rc;
+  const int n_pad = bwd_pad_rows(a.n);
+  float* L2 = static_cast<float*>(a.workspace);
+  float* Dv = L2 + static_cast<size_t>(a.B) * a.H * n_pad;
+  if (int rc = launch_bwd_pre_rows(bf16, a, L2, Dv, n_pad, s, err)) return rc;
   switch (a.d) {
-    case 16: rc = launch_bwd_tc_d16(bf16, a, Dv, acc, s, err); break;
-    case 32: rc = launch_bwd_tc_d32(bf16, a, Dv, acc, s, err); break;
-    case 64: rc = launch_bwd_tc_d64(bf16, a, Dv, acc, s, err); break;
-    case 128: rc = launch_bwd_tc_d128(bf16, a, Dv, acc, s, err); break;
+    case 16: return launch_bwd_tc_d16(bf16, a, L2, s, err);
+    case 32: return launch_bwd_tc_d32(bf16, a, L2, s, err);
+    case 64: return launch_bwd_tc_d64(bf16, a, L2, s, err);
+    case 128: return launch_bwd_tc_d128(bf16, a, L2, s, err);
     default: err = "head dimension must be 16, 32, 64 or 128"; return -2;
   }
-  if (rc) return rc;
-  return launch_bwd_post(bf16, a, acc, s, err);
 }
 }  // namespace ea

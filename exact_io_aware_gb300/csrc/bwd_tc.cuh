@@ -1,29 +1,31 @@
-// Backward pass of exact tiled softmax attention on the tcgen05 tensor cores (fp16 / bf16).
+// Backward pass, part 1 of 2: dK and dV on the tcgen05 tensor cores (fp16 / bf16).
 //
 // Follows the reverse procedure of "Exact tiled attention and memory-aware differentiation":
 // every score block is recomputed from Q and K, p_ij = exp(s_ij - LSE_i) uses the retained row
 // statistic, g_ij = p_ij (dO_i . V_j - D_i) with D_i = dO_i . O_i, and
-//   dV_j += p_ij dO_i,   dK_j += c g_ij Q_i,   dQ_i += c g_ij K_j.
+//   dV_j += p_ij dO_i,   dK_j += c g_ij Q_i.
+// The dQ_i += c g_ij K_j part is computed by the query-tile kernel in dq_tc.cuh, which
+// recomputes the same p and g; splitting keeps every product 128 x 128 (full tensor-core rate),
+// needs no float32 atomics, and leaves tensor memory to the four accumulators below.
 // No probability matrix is ever stored.
 //
-// One CTA owns a tile of 128 keys of one head and walks the query blocks that can reach it
+// One CTA owns a tile of 128 keys of one head and walks the 128-query blocks that can reach it
 // (all of them, those at or after the diagonal under the causal mask, or the nonempty ones
-// under a bitmap).  Per query block of BQ rows:
-//   Sᵀ  = K Qᵀ          (tensor memory, one key per lane)
-//   Pᵀ  = exp2(Sᵀ c log2e - LSE log2e)           softmax warps, written back as 16-bit
+// under a bitmap).  Per query block:
+//   Sᵀ  = K Qᵀ              (tensor memory, one key per lane, 128 query columns)
+//   Pᵀ  = exp2(Sᵀ c log2e - LSE log2e)   softmax warps; 16-bit, written over Sᵀ and kept in
+//                                         registers for the dS pass
 //   dPᵀ = V dOᵀ
-//   dSᵀ = Pᵀ (dPᵀ - D)                           softmax warps, to tensor and shared memory
-//   dV += Pᵀ dO,  dK += dSᵀ Q                    (A operand read from tensor memory)
-//   dQ  = dS K   (d <= 64)  or  dQᵀ = Kᵀ dSᵀ (d = 128, so the 128-lane accumulator holds d)
-// and dQ is added into a float32 accumulator in global memory; dK and dV stay in tensor memory
-// until the last block.  Roles:
-//   warps 0-7  softmax (P and dS): warp w owns TMEM lanes 32 (w % 4).. and half w / 4 of the
-//              block's query columns (P and dS are elementwise, so the halves never meet)
-//   warps 8-11 dQ reduction and dK/dV epilogue
-//   warp  12   TMA producer (K, V once; Q, dO per block through an NS-stage ring)
-//   warp  13   TMEM allocator and MMA issuer
-// With d = 128 a block has 64 queries and two S buffers, so S of the next block is computed
-// while the softmax warps still work on the current one.
+//   dSᵀ = Pᵀ (dPᵀ - D)                   softmax warps; 16-bit, written over dPᵀ
+//   dV += Pᵀ dO,  dK += dSᵀ Q            (A operand read from tensor memory)
+// Roles:
+//   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. and half w / 4 of the block's query
+//              columns (P and dS are elementwise, so the halves never meet); warps 0-3 also
+//              write dK and dV at the end
+//   warp  8    TMA producer (K, V once; Q, dO, LSE, D per block through an NS-stage ring)
+//   warp  9    TMEM allocator and MMA issuer
+// Issue order per block i: dV_i, S_{i+1}, dK_i, dP_{i+1}: S_{i+1} follows dV_i, the last reader
+// of P_i, and dP_{i+1} follows dK_i, the last reader of dS_i.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -35,11 +37,11 @@ namespace ea {
 namespace bwd {
 
 constexpr int kKeys = 128;
-constexpr int kThreads = 448;
-constexpr int kSoftmaxWarps = 8;  // two per TMEM lane quadrant, each on half the block's queries
-constexpr int kReduceWarp0 = 8;   // warps 8-11: dQ reduction and the dK/dV epilogue
-constexpr int kProducerWarp = 12;
-constexpr int kMmaWarp = 13;
+constexpr int BQ = 128;  // queries per block
+constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
 
 struct BwdParams {
@@ -49,62 +51,52 @@ struct BwdParams {
   const uint32_t* mask_bits;
   int64_t mask_row_words;
   int64_t mask_head_stride_words;
-  const float* lse;
+  // Row table [heads][n_pad] (n_pad = n rounded up to 128), written by the preprocessing
+  // step: L2 = LSE * log2(e), +inf where a row has no allowed key or lies past n; Dv = D_i,
+  // 0 past n.
+  const float* L2;
   const float* Dv;
-  float* dq_acc;
+  int n_pad;
   uint32_t* status;
 };
 
 __host__ __device__ constexpr int pad32(int x) { return x < 32 ? 32 : x; }
 
+// Column (within an S or dP buffer) of the 16-bit pair holding query column c.  Each half of
+// the block's queries packs its pairs at the start of its own fp32 column range, so the two
+// softmax warps sharing a lane quadrant never overwrite columns the other still reads.
+__host__ __device__ constexpr int packed_col(int c) {
+  return (c / (BQ / 2)) * (BQ / 2) + (c % (BQ / 2)) / 2;
+}
+
 template <int D>
 struct Config {
-  static constexpr bool kTr = D == 128;  // dQᵀ = Kᵀ dSᵀ
-  static constexpr int BQ = kTr ? 64 : 128;
-  using TK = Tile<kKeys, D>;   // K, V (and dK, dV staging)
-  using TQ = Tile<BQ, D>;      // Q, dO stages
-  using TS = Tile<kKeys, BQ>;  // dSᵀ: rows = keys, cols = queries
-  static constexpr int kDqCols = pad32(kTr ? BQ : D);
-  // One S buffer (P stays in the softmax warps' registers between its two passes, so S is free
-  // once dV has read P) and, where tensor memory allows, two dP buffers so dP of the next block
-  // is computed while the softmax warps still work on this one.
-  static constexpr int kTwoDP = BQ + 2 * BQ + kDqCols + 2 * pad32(D);
-  static constexpr int NDP = kTwoDP <= 512 ? 2 : 1;
-  // tensor-memory columns
+  using TK = Tile<kKeys, D>;  // K, V (and dK, dV staging)
+  using TQ = Tile<BQ, D>;     // Q, dO stages
+  // tensor-memory columns: S, dP, dV, dK
   static constexpr int kColS = 0;
-  static constexpr int kColDP = BQ;  // dP buffer b at kColDP + b * BQ
-  static constexpr int kColDV = kColDP + NDP * BQ;
+  static constexpr int kColDP = BQ;
+  static constexpr int kColDV = 2 * BQ;
   static constexpr int kColDK = kColDV + pad32(D);
-  static constexpr int kColDQ = kColDK + pad32(D);
-  static constexpr int kTmemCols = kColDQ + kDqCols;
+  static constexpr int kTmemCols = kColDK + pad32(D);
   static_assert(kTmemCols <= 512, "tensor memory overflow");
-  static constexpr int kTmemAlloc = kTmemCols <= 128 ? 128 : kTmemCols <= 256 ? 256 : 512;
-  using TDQ = F32Tile<BQ, D>;  // float32 dQ block staged for the TMA reduce-add
-  // Shared memory: K, V, NDS dSᵀ buffers, dQ staging, then NS stages of (Q, dO, LSE, D).
-  // A third Q/dO stage matters more than a second dSᵀ buffer: the load of block i+1 can then
-  // start when block i-2 releases its stage, a whole block earlier than with two stages.
+  static constexpr int kTmemAlloc = kTmemCols <= 256 ? 256 : 512;
+  // shared memory: K, V, then NS stages of (Q, dO, LSE, D), the step table, and (bitmap masks)
+  // each stage's allowed-key words
   static constexpr int kBudget = 227 * 1024 - 2048;
-  // per stage: Q, dO, LSE, D (bitmap masks add the block's allowed-key words after the step
-  // table, sized per launch)
   static constexpr int kStage = 2 * TQ::kBytes + 2 * BQ * 4;
-  static constexpr int kMaxStepBytes = 4 * 1024;  // n <= 65536 at BQ = 64
-  static constexpr int kFixed1 = 2 * TK::kBytes + TS::kBytes + TDQ::kBytes;
-  static constexpr int kFit1 = (kBudget - kFixed1 - TS::kBytes - kMaxStepBytes) / kStage;
-  static constexpr int NDS = kFit1 >= 3 ? 2 : 1;
-  static constexpr int kFixed = kFixed1 + (NDS - 1) * TS::kBytes;
-  static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes) / kStage;
+  static constexpr int kMaxStepBytes = 4 * 1024;
+  static constexpr int kFixed = 2 * TK::kBytes;
+  static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes - 4 * BQ * 16) / kStage;
   static constexpr int NS = kFit > 4 ? 4 : kFit;
-  static_assert(NS >= 3, "need three query stages");
+  static_assert(NS >= 2, "need two query stages");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + TK::kBytes;
-  static constexpr int kOffDS = kOffV + TK::kBytes;
-  static constexpr int kOffDQ = kOffDS + NDS * TS::kBytes;
-  static constexpr int kOffQ = kOffDQ + TDQ::kBytes;
+  static constexpr int kOffQ = kOffV + TK::kBytes;
   static constexpr int kOffG = kOffQ + NS * TQ::kBytes;
   static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [NS][BQ] LSE (log2 units)
   static constexpr int kOffD = kOffL + NS * BQ * 4;      // [NS][BQ] D
   static constexpr int kOffSteps = kOffD + NS * BQ * 4;
-  // [NS][BQ][4] mask words, after the step table (bitmap masks only)
   __host__ __device__ static constexpr int off_bits(int n) {
     return (kOffSteps + 4 * ((n + BQ - 1) / BQ) + 15) / 16 * 16;
   }
@@ -116,10 +108,7 @@ struct Config {
 struct Barriers {
   uint64_t kv_full;
   uint64_t qdo_full[4], qdo_empty[4], ld_full[4];
-  uint64_t s_full;
-  uint64_t p_full, dp_full[2], ds_full[2];
-  uint64_t dss_free[2];
-  uint64_t dq_full, dq_free;
+  uint64_t s_full, p_full, dp_full, ds_full;
   uint64_t kv_done;
   uint32_t tmem_base;
   uint32_t nsteps;
@@ -131,14 +120,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// Column (within an S or dP buffer) of the 16-bit pair holding query column c.  Each half of
-// the block's queries packs its pairs at the start of its own fp32 column range, so the two
-// softmax warps sharing a lane quadrant never overwrite columns the other still reads.
-template <int BQ>
-__host__ __device__ constexpr int packed_col(int c) {
-  return (c / (BQ / 2)) * (BQ / 2) + (c % (BQ / 2)) / 2;
 }
 
 template <bool kBf16>
@@ -159,23 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                  const __grid_constant__ CUtensorMap tm_dq, BwdParams p) {
+                  BwdParams p) {
   using C = Config<D>;
   using TK = typename C::TK;
   using TQ = typename C::TQ;
-  using TS = typename C::TS;
-  using TDQ = typename C::TDQ;
-  constexpr int BQ = C::BQ;
   constexpr int NS = C::NS;
-  constexpr int NDP = C::NDP;
-  constexpr int NDS = C::NDS;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
-  uint8_t* sDS = smem + C::kOffDS;
-  uint8_t* sDQ = smem + C::kOffDQ;
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sG = smem + C::kOffG;
   float* sL = reinterpret_cast<float*>(smem + C::kOffL);
@@ -200,18 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.qdo_empty[s], 1);
       mbar_init(&bars.ld_full[s], 32);
     }
-    // ds_full is per dP buffer: dP of the next block is issued before this block's dS is
-    // published, so a fast softmax warp may publish dS of the next block before a slow warp has
-    // published this one, and a single barrier would count that arrival towards the wrong phase.
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.p_full, kSoftmaxWarps);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars.dss_free[b], 1);
-      mbar_init(&bars.dp_full[b], 1);
-      mbar_init(&bars.ds_full[b], kSoftmaxWarps);
-    }
-    mbar_init(&bars.dq_full, 1);
-    mbar_init(&bars.dq_free, 4);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ds_full, kSoftmaxWarps);
     mbar_init(&bars.kv_done, 1);
     fence_barrier_init();
   }
@@ -280,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
     // Lane 0 issues the TMA loads; all lanes stage each block's LSE (log2 units, +inf for
-    // rows past n or with an empty allowed set) and D into shared memory.
-    const float* lse_h = p.lse + static_cast<int64_t>(bh) * n;
-    const float* d_h = p.Dv + static_cast<int64_t>(bh) * n;
+    // rows past n or with an empty allowed set), D and, for bitmap masks, allowed-key words.
+    const float* l2_h = p.L2 + static_cast<int64_t>(bh) * p.n_pad;
+    const float* d_h = p.Dv + static_cast<int64_t>(bh) * p.n_pad;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_g);
@@ -307,11 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                       b * TQ::L::kBoxCols, q0, bh);
         }
       }
-      for (int t = lane; t < BQ; t += 32) {
-        const int q = q0 + t;
-        const float lv = q < n ? __ldg(lse_h + q) : -INFINITY;
-        sL[s * BQ + t] = lv == -INFINITY ? INFINITY : lv * 1.4426950408889634f;
-        sD[s * BQ + t] = q < n ? __ldg(d_h + q) : 0.0f;
+      if (lane == 0) {
+        // rows q0 .. q0+BQ-1 of the row table (always inside the padded table)
+        mbar_expect_tx(&bars.ld_full[s], 2 * BQ * 4);
+        bulk_load(sL + s * BQ, l2_h + q0, BQ * 4, &bars.ld_full[s]);
+        bulk_load(sD + s * BQ, d_h + q0, BQ * 4, &bars.ld_full[s]);
       }
       if (p.mask_kind == kMaskBitmap && ((steps[i] >> 16) & 3u) == kPartial) {
         // words of allowed-key bits for rows q0.. of this block and keys key0..key0+127;
@@ -334,10 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);   // Sᵀ, dPᵀ
-      constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dV, dK
-      constexpr uint32_t id_q = C::kTr ? idesc_f16(D, BQ, kBf16 ? 1 : 0, 1, 1)
-                                       : idesc_f16(BQ, D, kBf16 ? 1 : 0, 1, 1);
+      constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);  // Sᵀ, dPᵀ
+      constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);  // dV, dK
       const uint32_t sk = smem_u32(sK), sv = smem_u32(sV);
       bool ok = mbar_wait(&bars.kv_full, 0, p.status, 22);
       auto wait_qdo = [&](int i) -> bool {
@@ -354,9 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t gb = smem_u32(sG + (i % NS) * TQ::kBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP + (i % NDP) * BQ, TK::desc_k(sv, kk), TQ::desc_k(gb, kk), id_s,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(&bars.dp_full[i % NDP]);
+          mma_ss(tmem + C::kColDP, TK::desc_k(sv, kk), TQ::desc_k(gb, kk), id_s, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.dp_full);
       };
       if (ok && nsteps > 0) {
         ok = wait_qdo(0);
@@ -366,62 +329,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_dp(0);
         }
       }
-      // Order per block i: [dP_{i+1}], dV_i, S_{i+1}, dK_i, [dP_{i+1}], dQ_i.  With two dP
-      // buffers dP_{i+1} goes first, so the softmax warps find it ready when they finish dS_i;
-      // S_{i+1} follows dV_i, the last reader of P_i in the (single) S buffer.
       for (int i = 0; i < nsteps && ok; ++i) {
         const int s = i % NS;
         const uint32_t qb = smem_u32(sQ + s * TQ::kBytes);
         const uint32_t gb = smem_u32(sG + s * TQ::kBytes);
-        if (NDP == 2 && i + 1 < nsteps) {
-          ok = wait_qdo(i + 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_dp(i + 1);
-        }
         ok = mbar_wait(&bars.p_full, i & 1, p.status, 24);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col<BQ>(16 * kk), TQ::desc_mn(gb, kk),
-                 id_kv, (i > 0 || kk > 0) ? 1u : 0u);
-        if (i + 1 < nsteps) {
-          if (NDP == 1) {
-            ok = wait_qdo(i + 1);
-            if (!ok) break;
-            tc_fence_after();
-          }
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), TQ::desc_mn(gb, kk), id_kv,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        const bool more = i + 1 < nsteps;
+        if (more) {
+          ok = wait_qdo(i + 1);
+          if (!ok) break;
+          tc_fence_after();
           issue_s(i + 1);
         }
-        ok = mbar_wait(&bars.ds_full[i % NDP], (i / NDP) & 1, p.status, 25);
+        ok = mbar_wait(&bars.ds_full, i & 1, p.status, 25);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + (i % NDP) * BQ + packed_col<BQ>(16 * kk),
-                 TQ::desc_mn(qb, kk), id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(16 * kk), TQ::desc_mn(qb, kk), id_kv,
+                 (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.qdo_empty[s]);
-        if (NDP == 1 && i + 1 < nsteps) issue_dp(i + 1);
-        ok = mbar_wait(&bars.dq_free, (i & 1) ^ 1, p.status, 26);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t dsb = smem_u32(sDS + (i % NDS) * TS::kBytes);
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          if constexpr (C::kTr)
-            mma_ss(tmem + C::kColDQ, TK::desc_mn(sk, kk), TS::desc_mn(dsb, kk), id_q,
-                   kk > 0 ? 1u : 0u);
-          else
-            mma_ss(tmem + C::kColDQ, TS::desc_mn(dsb, kk), TK::desc_mn(sk, kk), id_q,
-                   kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&bars.dq_full);
-        mma_commit(&bars.dss_free[i % NDS]);
+        if (more) issue_dp(i + 1);
       }
       mma_commit(&bars.kv_done);
     }
-  } else if (warp < kSoftmaxWarps) {
+  } else {
     // ---------------------------------------------------------------- softmax: P and dS
     const int quad = warp % 4;
     const int r = quad * 32 + lane;  // key row within the tile = TMEM lane
@@ -430,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kHalf = BQ / 2;  // query columns of this warp: [c_lo, c_lo + kHalf)
     const int c_lo = (warp / 4) * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
+    const uint32_t tS = tmem + C::kColS + lane_off;
+    const uint32_t tP = tmem + C::kColDP + lane_off;
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
@@ -441,8 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait(&bars.s_full, i & 1, p.status, 27);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem + C::kColS + lane_off;
-      const uint32_t tP = tmem + C::kColDP + (i % NDP) * BQ + lane_off;
       uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
@@ -477,140 +415,79 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
           pkeep[cc / 2 + k] = pk[k];
         }
-        tmem_st16(tS + packed_col<BQ>(c0), pk);
+        tmem_st16(tS + packed_col(c0), pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full);
 
-      ok = mbar_wait(&bars.dp_full[i % NDP], (i / NDP) & 1, p.status, 28);
-      if (ok && i >= NDS)
-        ok = mbar_wait(&bars.dss_free[i % NDS], ((i / NDS) & 1) ^ 1, p.status, 29);
+      ok = mbar_wait(&bars.dp_full, i & 1, p.status, 28);
       if (!ok) break;
       tc_fence_after();
-      uint8_t* ds_tile = sDS + (i % NDS) * TS::kBytes;
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
         uint32_t dp[32];
         tmem_ld32(tP + c0, dp);
         tmem_wait_ld();
-        const uint32_t* pp = pkeep + cc / 2;
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
-          unpack2<kBf16>(pp[k], p0, p1);
+          unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
           const float g0 = p0 * (__uint_as_float(dp[2 * k]) - Dd[c0 + 2 * k]);
           const float g1 = p1 * (__uint_as_float(dp[2 * k + 1]) - Dd[c0 + 2 * k + 1]);
           pk[k] = pack2<kBf16>(g0, g1);
         }
-        tmem_st16(tP + packed_col<BQ>(c0), pk);
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(ds_tile + TS::offset(r, c0 + 8 * u)) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        tmem_st16(tP + packed_col(c0), pk);
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.ds_full[i % NDP]);
+      if (lane == 0) mbar_arrive(&bars.ds_full);
     }
-  } else {
-    // ---------------------------------------------------------------- dQ reduction, epilogue
-    const int quad = warp - kReduceWarp0;
-    const int r = quad * 32 + lane;  // TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    // Each block's dQ leaves tensor memory through a swizzled float32 staging tile and one
-    // TMA reduce-add per 32-column box into the float32 accumulator (rows past n are dropped
-    // by the tensor map).  Tensor memory is released before the shared-memory copy is done.
-    bool ok = true;
-    for (int i = 0; i < nsteps && ok; ++i) {
-      const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
-      ok = mbar_wait(&bars.dq_full, i & 1, p.status, 30);
-      if (!ok) break;
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
+    if (warp < 4) {
+      if (ok) ok = mbar_wait(&bars.kv_done, 0, p.status, 31);
       tc_fence_after();
-      if (i > 0) {
-        if (r == 0) tma_store_wait_read();  // the previous block's reduce has read the tile
-        named_barrier(2, 128);
-      }
-      if constexpr (C::kTr) {
-        // lane = column a of dQ (a < D = 128), columns = the block's queries
-#pragma unroll
-        for (int c0 = 0; c0 < BQ; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tmem + C::kColDQ + lane_off + c0, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            *reinterpret_cast<uint32_t*>(sDQ + TDQ::offset(c0 + k, r)) = rr[k];
-        }
-      } else {
-        // lane = query of the block, columns = dQ columns
+      if (ok) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t rr[16];
-          tmem_ld16(tmem + C::kColDQ + lane_off + c0, rr);
-          tmem_wait_ld();
+          uint32_t rv[16], rk[16];
+          if (nsteps > 0) {
+            tmem_ld16(tmem + C::kColDV + lane_off + c0, rv);
+            tmem_ld16(tmem + C::kColDK + lane_off + c0, rk);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(sDQ + TDQ::offset(r, c0 + 4 * u)) =
-                make_uint4(rr[4 * u], rr[4 * u + 1], rr[4 * u + 2], rr[4 * u + 3]);
+            for (int k = 0; k < 16; ++k) rv[k] = rk[k] = 0u;
+          }
+          uint32_t pv[8], pkk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            pv[k] = pack2<kBf16>(__uint_as_float(rv[2 * k]), __uint_as_float(rv[2 * k + 1]));
+            pkk[k] = pack2<kBf16>(p.c * __uint_as_float(rk[2 * k]), p.c * __uint_as_float(rk[2 * k + 1]));
+          }
+          *reinterpret_cast<uint4*>(sV + TK::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+          *reinterpret_cast<uint4*>(sV + TK::offset(r, c0 + 8)) = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+          *reinterpret_cast<uint4*>(sK + TK::offset(r, c0)) = make_uint4(pkk[0], pkk[1], pkk[2], pkk[3]);
+          *reinterpret_cast<uint4*>(sK + TK::offset(r, c0 + 8)) =
+              make_uint4(pkk[4], pkk[5], pkk[6], pkk[7]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.dq_free);
       fence_proxy_async_smem();
       named_barrier(2, 128);
-      if (r == 0) {
+      if (ok && r == 0) {
 #pragma unroll
-        for (int b = 0; b < TDQ::kBoxes; ++b)
-          tma_reduce_add_3d(&tm_dq, sDQ + b * TDQ::kBoxBytes, b * TDQ::kBoxCols, q0, bh);
+        for (int b = 0; b < TK::L::kBoxes; ++b) {
+          tma_store_3d(&tm_dk, sK + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
+          tma_store_3d(&tm_dv, sV + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
+        }
         tma_store_commit();
+        tma_store_wait_all();
       }
-    }
-    if (r == 0) tma_store_wait_all();
-    // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
-    if (ok) ok = mbar_wait(&bars.kv_done, 0, p.status, 31);
-    tc_fence_after();
-    if (ok) {
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        uint32_t rv[16], rk[16];
-        if (nsteps > 0) {
-          tmem_ld16(tmem + C::kColDV + lane_off + c0, rv);
-          tmem_ld16(tmem + C::kColDK + lane_off + c0, rk);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int k = 0; k < 16; ++k) rv[k] = rk[k] = 0u;
-        }
-        uint32_t pv[8], pkk[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          pv[k] = pack2<kBf16>(__uint_as_float(rv[2 * k]), __uint_as_float(rv[2 * k + 1]));
-          pkk[k] = pack2<kBf16>(p.c * __uint_as_float(rk[2 * k]), p.c * __uint_as_float(rk[2 * k + 1]));
-        }
-        *reinterpret_cast<uint4*>(sV + TK::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-        *reinterpret_cast<uint4*>(sV + TK::offset(r, c0 + 8)) = make_uint4(pv[4], pv[5], pv[6], pv[7]);
-        *reinterpret_cast<uint4*>(sK + TK::offset(r, c0)) = make_uint4(pkk[0], pkk[1], pkk[2], pkk[3]);
-        *reinterpret_cast<uint4*>(sK + TK::offset(r, c0 + 8)) =
-            make_uint4(pkk[4], pkk[5], pkk[6], pkk[7]);
-      }
-    }
-    fence_proxy_async_smem();
-    named_barrier(2, 128);
-    if (ok && r == 0) {
-#pragma unroll
-      for (int b = 0; b < TK::L::kBoxes; ++b) {
-        tma_store_3d(&tm_dk, sK + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
-        tma_store_3d(&tm_dv, sV + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
-      }
-      tma_store_commit();
-      tma_store_wait_all();
     }
   }
 

@@ -1,9 +1,8 @@
-// tcgen05 backward kernels for head dimension 16.
+// tcgen05 backward kernels (dK/dV and dQ) for head dimension 16.
 #include "bwd_tc_launch.cuh"
 
 namespace ea {
-int launch_bwd_tc_d16(bool bf16, const AttnArgs& a, float* Dv, float* acc, cudaStream_t s,
-                      std::string& err) {
-  return bf16 ? bwd::run<true, 16>(a, Dv, acc, s, err) : bwd::run<false, 16>(a, Dv, acc, s, err);
+int launch_bwd_tc_d16(bool bf16, const AttnArgs& a, const float* L2, cudaStream_t s, std::string& err) {
+  return bf16 ? bwd::run<true, 16>(a, L2, s, err) : bwd::run<false, 16>(a, L2, s, err);
 }
 }  // namespace ea

@@ -1,9 +1,8 @@
-// tcgen05 backward kernels for head dimension 64.
+// tcgen05 backward kernels (dK/dV and dQ) for head dimension 64.
 #include "bwd_tc_launch.cuh"
 
 namespace ea {
-int launch_bwd_tc_d64(bool bf16, const AttnArgs& a, float* Dv, float* acc, cudaStream_t s,
-                      std::string& err) {
-  return bf16 ? bwd::run<true, 64>(a, Dv, acc, s, err) : bwd::run<false, 64>(a, Dv, acc, s, err);
+int launch_bwd_tc_d64(bool bf16, const AttnArgs& a, const float* L2, cudaStream_t s, std::string& err) {
+  return bf16 ? bwd::run<true, 64>(a, L2, s, err) : bwd::run<false, 64>(a, L2, s, err);
 }
 }  // namespace ea

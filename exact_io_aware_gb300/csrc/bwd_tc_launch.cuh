@@ -1,6 +1,8 @@
-// Host launcher for the tcgen05 backward kernel (instantiated per head dimension).
+// Host launchers of the tcgen05 backward kernels (dK/dV by key tiles, dQ by query tiles),
+// instantiated per head dimension.
 #pragma once
 #include "bwd_tc.cuh"
+#include "dq_tc.cuh"
 #include "tmap.h"
 
 namespace ea {
@@ -9,40 +11,53 @@ namespace bwd {
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 
 template <bool kBf16, int D>
-int run(const AttnArgs& a, float* Dv, float* acc, cudaStream_t s, std::string& err) {
+int run(const AttnArgs& a, const float* L2, cudaStream_t s, std::string& err) {
   using Cfg = Config<D>;
-  const size_t smem = Cfg::smem_bytes(a.n, a.mask_kind == kMaskBitmap);
-  if (smem > static_cast<size_t>(kMaxDynSmem)) {
-    err = "n too large for the backward step table";
+  using QCfg = dq::Config<D>;
+  const bool bitmap = a.mask_kind == kMaskBitmap;
+  const size_t smem = Cfg::smem_bytes(a.n, bitmap);
+  const size_t qsmem = QCfg::smem_bytes(a.n);
+  if (smem > static_cast<size_t>(kMaxDynSmem) || qsmem > static_cast<size_t>(kMaxDynSmem)) {
+    err = "n too large for the backward step tables";
     return -2;
   }
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;
   constexpr uint32_t bc = RowLayout<D>::kBoxCols;
   CUtensorMap tq, tk, tv, tg, tdk, tdv, tdq;
-  if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, Cfg::BQ, bc) ||
-      !encode_tile_map(&tg, a.d_o, kBf16, heads, a.n, D, Cfg::BQ, bc) ||
-      !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, kKeys, bc) ||
-      !encode_tile_map(&tv, a.v, kBf16, heads, a.n, D, kKeys, bc) ||
-      !encode_tile_map(&tdk, a.dk, kBf16, heads, a.n, D, kKeys, bc) ||
-      !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, D, kKeys, bc) ||
-      !encode_f32_map(&tdq, acc, heads, a.n, D, Cfg::BQ, Cfg::TDQ::kBoxCols)) {
+  if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tg, a.d_o, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tv, a.v, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tdk, a.dk, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tdq, a.dq, kBf16, heads, a.n, D, 128, bc)) {
     err = "cuTensorMapEncodeTiled rejected a backward tensor map";
     return -5;
   }
+  const int n_pad = bwd_pad_rows(a.n);
+  BwdParams p{a.n,  a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
+              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.status};
+  const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
   auto kern = bwd_tc_kernel<kBf16, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, tg, tdk, tdv, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) {
-    err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+    err = std::string("dK/dV launch: ") + cudaGetErrorString(e);
     return -5;
   }
-  BwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
-              a.lse, Dv, acc, a.status};
-  dim3 grid((a.n + kKeys - 1) / kKeys, static_cast<unsigned>(heads));
-  kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, tg, tdk, tdv, tdq, p);
-  e = cudaGetLastError();
+  auto qkern = dq::dq_tc_kernel<kBf16, D>;
+  e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(qsmem));
+  if (e == cudaSuccess) {
+    qkern<<<grid, dq::kThreads, qsmem, s>>>(tq, tk, tv, tg, tdq, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) {
-    err = std::string("backward launch: ") + cudaGetErrorString(e);
+    err = std::string("dQ launch: ") + cudaGetErrorString(e);
     return -5;
   }
   return 0;

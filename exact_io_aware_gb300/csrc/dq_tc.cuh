@@ -1,0 +1,401 @@
+// Backward pass, part 2 of 2: dQ on the tcgen05 tensor cores (fp16 / bf16).
+//
+// The query-row side of the reverse procedure of "Exact tiled attention and memory-aware
+// differentiation": for each query row i and allowed key j, recompute s_ij from Q and K,
+// p_ij = exp(s_ij - LSE_i), g_ij = p_ij (dO_i . V_j - D_i), and accumulate
+//   dQ_i += c g_ij K_j.
+// (dK and dV come from the key-tile kernel in bwd_tc.cuh, which recomputes the same p and g.)
+//
+// One CTA owns a tile of 128 query rows of one head and walks the 128-key blocks they reach,
+// exactly like the forward; LSE_i and D_i are per-row scalars held by the row's thread.
+// Per key block j:
+//   S  = Q K_jᵀ           (tensor memory, one query row per lane; two buffers)
+//   P  = exp2(S c log2e - LSE log2e)     softmax warps, kept in registers
+//   dP = dO V_jᵀ
+//   dS = P (dP - D)                      softmax warps; 16-bit, written over dP
+//   dQ += dS K_j                         (A operand read from tensor memory)
+// Roles:
+//   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. and half w / 4 of the block's key
+//              columns; warps 0-3 also write dQ at the end
+//   warp  8    TMA producer (Q, dO once; K and V blocks through an NS-stage ring)
+//   warp  9    TMEM allocator and MMA issuer
+// Issue order per block i: [S_{i+1}], dQ_i, [dP_{i+1}]: dP_{i+1} follows dQ_i, the last reader
+// of dS_i.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "bwd_tc.cuh"
+
+namespace ea {
+namespace dq {
+
+constexpr int kRows = 128;  // query rows per CTA
+constexpr int BN = 128;     // keys per block
+constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+using bwd::kFull;
+using bwd::kPartial;
+using bwd::kSkip;
+using bwd::packed_col;
+using bwd::pad32;
+using bwd::unpack2;
+
+template <int D>
+struct Config {
+  using TQ = Tile<kRows, D>;  // Q, dO (and dQ staging)
+  using TK = Tile<BN, D>;     // K, V stages
+  // tensor-memory columns: S buffers, dP, dQ
+  static constexpr int kColS = 0;  // buffer b at b * BN
+  static constexpr int kColDP = 2 * BN;
+  static constexpr int kColDQ = 3 * BN;
+  static constexpr int kTmemCols = kColDQ + pad32(D);
+  static_assert(kTmemCols <= 512, "tensor memory overflow");
+  static constexpr int kTmemAlloc = 512;
+  static constexpr int kBudget = 227 * 1024 - 2048;
+  static constexpr int kMaxStepBytes = 4 * 1024;
+  static constexpr int kFixed = 2 * TQ::kBytes;
+  static constexpr int kStage = 2 * TK::kBytes;
+  static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes) / kStage;
+  static constexpr int NS = kFit > 4 ? 4 : kFit;
+  static_assert(NS >= 2, "need two key stages");
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffG = kOffQ + TQ::kBytes;
+  static constexpr int kOffK = kOffG + TQ::kBytes;
+  static constexpr int kOffV = kOffK + NS * TK::kBytes;
+  static constexpr int kOffSteps = kOffV + NS * TK::kBytes;
+  static size_t smem_bytes(int n) {
+    return 1024 + kOffSteps + 4 * static_cast<size_t>((n + BN - 1) / BN);
+  }
+};
+
+struct Barriers {
+  uint64_t qg_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[2], dp_full, ds_full;
+  uint64_t dq_done;
+  uint32_t tmem_base;
+  uint32_t nsteps;
+};
+
+template <bool kBf16, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                 const __grid_constant__ CUtensorMap tm_dq, bwd::BwdParams p) {
+  using C = Config<D>;
+  using TQ = typename C::TQ;
+  using TK = typename C::TK;
+  constexpr int NS = C::NS;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = bwd::align1024(smem_raw);
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sG = smem + C::kOffG;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
+  uint32_t* steps = reinterpret_cast<uint32_t*>(smem + C::kOffSteps);
+  __shared__ Barriers bars;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int n = p.n;
+  const int bh = blockIdx.y;
+  const int tile = gridDim.x - 1 - blockIdx.x;  // heaviest (causal) query tiles first
+  const int row0 = tile * kRows;
+  const int nblk = (n + BN - 1) / BN;
+
+  // ---------------------------------------------------------------- prologue
+  if (tid == 0) {
+    mbar_init(&bars.qg_full, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    mbar_init(&bars.s_full[0], 1);
+    mbar_init(&bars.s_full[1], 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ds_full, kSoftmaxWarps);
+    mbar_init(&bars.dq_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
+
+  // Classify each key block for this query tile: skip / full / partial (mask needed).
+  for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
+  __syncthreads();
+  const int last_row = min(row0 + kRows, n) - 1;
+  if (p.mask_kind == kMaskBitmap) {
+    if (tid < kRows) {
+      const int row = row0 + tid;
+      const bool valid = row < n;
+      const uint32_t* rowbits = p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
+                                static_cast<int64_t>(valid ? row : 0) * p.mask_row_words;
+      for (int j = 0; j < nblk; ++j) {
+        bool any = false, all = true;
+        if (valid) {
+#pragma unroll
+          for (int q = 0; q < BN / 32; ++q) {
+            const int key0 = j * BN + q * 32;
+            if (key0 < n) {
+              uint32_t w = __ldg(rowbits + key0 / 32);
+              const int nk = n - key0;
+              const uint32_t live = nk >= 32 ? 0xFFFFFFFFu : ((1u << nk) - 1u);
+              w &= live;
+              any |= w != 0;
+              all &= w == live;
+            }
+          }
+        }
+        const bool wany = __any_sync(0xFFFFFFFFu, any);
+        const bool wall = __all_sync(0xFFFFFFFFu, all);
+        if (lane == 0) {
+          const uint32_t bits = (wany ? 1u : 0u) | (wall ? 0u : 2u);
+          if (bits) atomicOr(&steps[j], bits);
+        }
+      }
+    }
+  } else if (row0 < n) {
+    for (int j = tid; j < nblk; j += kThreads) {
+      bool any = true, all = true;
+      if (p.mask_kind == kMaskCausal) {
+        any = j * BN <= last_row;
+        all = (j + 1) * BN - 1 <= row0;
+      }
+      steps[j] = any ? (1u | (all ? 0u : 2u)) : 0u;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int ns = 0;
+    for (int j = 0; j < nblk; ++j) {
+      const uint32_t b = steps[j];
+      if (!(b & 1u)) continue;
+      const bool tail = (j + 1) * BN > n || row0 + kRows > n;
+      const uint32_t cls = ((b & 2u) || tail) ? kPartial : kFull;
+      steps[ns++] = static_cast<uint32_t>(j) | (cls << 16);
+    }
+    bars.nsteps = ns;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int nsteps = bars.nsteps;
+  const uint32_t tmem = bars.tmem_base;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && nsteps > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&bars.qg_full, 2 * TQ::kBytes);
+#pragma unroll
+      for (int b = 0; b < TQ::L::kBoxes; ++b) {
+        tma_load_3d(sQ + b * TQ::kBoxBytes, &tm_q, &bars.qg_full, b * TQ::L::kBoxCols, row0, bh);
+        tma_load_3d(sG + b * TQ::kBoxBytes, &tm_g, &bars.qg_full, b * TQ::L::kBoxCols, row0, bh);
+      }
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % NS;
+        const uint32_t ph = (i / NS) & 1;
+        const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
+        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, p.status, 42)) break;
+        mbar_arrive_expect_tx(&bars.k_full[s], TK::kBytes);
+#pragma unroll
+        for (int b = 0; b < TK::L::kBoxes; ++b)
+          tma_load_3d(sK + s * TK::kBytes + b * TK::kBoxBytes, &tm_k, &bars.k_full[s],
+                      b * TK::L::kBoxCols, key0, bh);
+        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, p.status, 41)) break;
+        mbar_arrive_expect_tx(&bars.v_full[s], TK::kBytes);
+#pragma unroll
+        for (int b = 0; b < TK::L::kBoxes; ++b)
+          tma_load_3d(sV + s * TK::kBytes + b * TK::kBoxBytes, &tm_v, &bars.v_full[s],
+                      b * TK::L::kBoxCols, key0, bh);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);  // S, dP
+      constexpr uint32_t id_q = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dQ
+      const uint32_t qb = smem_u32(sQ), gb = smem_u32(sG);
+      bool ok = nsteps == 0 || mbar_wait(&bars.qg_full, 0, p.status, 43);
+      auto issue_s = [&](int i) -> bool {
+        if (!mbar_wait(&bars.k_full[i % NS], (i / NS) & 1, p.status, 44)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sK + (i % NS) * TK::kBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColS + (i & 1) * BN, TQ::desc_k(qb, kk), TK::desc_k(kb, kk), id_s,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&bars.s_full[i & 1]);
+        return true;
+      };
+      auto issue_dp = [&](int i) -> bool {
+        if (!mbar_wait(&bars.v_full[i % NS], (i / NS) & 1, p.status, 45)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(sV + (i % NS) * TK::kBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColDP, TQ::desc_k(gb, kk), TK::desc_k(vb, kk), id_s, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.dp_full);
+        mma_commit(&bars.v_empty[i % NS]);
+        return true;
+      };
+      if (ok && nsteps > 0) ok = issue_s(0) && issue_dp(0);
+      for (int i = 0; i < nsteps && ok; ++i) {
+        const bool more = i + 1 < nsteps;
+        if (more) ok = issue_s(i + 1);
+        if (!ok) break;
+        ok = mbar_wait(&bars.ds_full, i & 1, p.status, 46);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sK + (i % NS) * TK::kBytes);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(16 * kk), TK::desc_mn(kb, kk),
+                 id_q, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.k_empty[i % NS]);
+        if (more) ok = issue_dp(i + 1);
+      }
+      mma_commit(&bars.dq_done);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax: P and dS
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;  // query row within the tile = TMEM lane
+    const int row = row0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    constexpr int kHalf = BN / 2;  // key columns of this warp: [c_lo, c_lo + kHalf)
+    const int c_lo = (warp / 4) * kHalf;
+    const float sl2 = p.c * 1.4426950408889634f;
+    // rows past n or with no allowed key carry +inf here, so their probabilities are 0
+    const float lse_l2 = __ldg(p.L2 + static_cast<int64_t>(bh) * p.n_pad + row);
+    const float dd = __ldg(p.Dv + static_cast<int64_t>(bh) * p.n_pad + row);
+    const uint32_t* rowbits =
+        p.mask_kind == kMaskBitmap
+            ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
+                  static_cast<int64_t>(row < n ? row : 0) * p.mask_row_words
+            : nullptr;
+    const uint32_t tP = tmem + C::kColDP + lane_off;
+    bool ok = true;
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
+      const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
+      uint32_t mword[kHalf / 32];
+      if (partial && p.mask_kind == kMaskBitmap) {
+#pragma unroll
+        for (int q = 0; q < kHalf / 32; ++q) {
+          const int kq = key0 + c_lo + q * 32;
+          uint32_t w = (row < n && kq < n) ? __ldg(rowbits + kq / 32) : 0u;
+          const int nk = n - kq;
+          if (nk < 32) w &= nk > 0 ? (1u << nk) - 1u : 0u;
+          mword[q] = w;
+        }
+      }
+      ok = mbar_wait(&bars.s_full[i & 1], (i >> 1) & 1, p.status, 47);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + C::kColS + (i & 1) * BN + lane_off;
+      uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
+#pragma unroll
+      for (int cc = 0; cc < kHalf; cc += 32) {
+        const int c0 = c_lo + cc;
+        uint32_t rr[32];
+        tmem_ld32(tS + c0, rr);
+        tmem_wait_ld();
+        float pv[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[k]) * sl2 - lse_l2);
+        if (partial) {
+          if (p.mask_kind == kMaskBitmap) {
+            const uint32_t w = mword[cc / 32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              if (!((w >> k) & 1u)) pv[k] = 0.0f;
+          } else {
+            const bool causal = p.mask_kind == kMaskCausal;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int key = key0 + c0 + k;
+              if (key >= n || (causal && key > row)) pv[k] = 0.0f;
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pkeep[cc / 2 + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
+      }
+      ok = mbar_wait(&bars.dp_full, i & 1, p.status, 48);
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int cc = 0; cc < kHalf; cc += 32) {
+        const int c0 = c_lo + cc;
+        uint32_t dp[32];
+        tmem_ld32(tP + c0, dp);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float p0, p1;
+          unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
+          pk[k] = pack2<kBf16>(p0 * (__uint_as_float(dp[2 * k]) - dd),
+                               p1 * (__uint_as_float(dp[2 * k + 1]) - dd));
+        }
+        tmem_st16(tP + packed_col(c0), pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.ds_full);
+    }
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // dQ = c * (dS K) rounded and stored through the (now idle) Q tile.
+    if (warp < 4 && row0 < n) {
+      if (ok && nsteps > 0) ok = mbar_wait(&bars.dq_done, 0, p.status, 49);
+      tc_fence_after();
+      if (ok) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t rr[16];
+          if (nsteps > 0) {
+            tmem_ld16(tmem + C::kColDQ + lane_off + c0, rr);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) rr[k] = 0u;
+          }
+          uint32_t pk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pk[k] = pack2<kBf16>(p.c * __uint_as_float(rr[2 * k]), p.c * __uint_as_float(rr[2 * k + 1]));
+          *reinterpret_cast<uint4*>(sQ + TQ::offset(r, c0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(sQ + TQ::offset(r, c0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      fence_proxy_async_smem();
+      bwd::named_barrier(2, 128);
+      if (ok && r == 0) {
+#pragma unroll
+        for (int b = 0; b < TQ::L::kBoxes; ++b)
+          tma_store_3d(&tm_dq, sQ + b * TQ::kBoxBytes, b * TQ::L::kBoxCols, row0, bh);
+        tma_store_commit();
+        tma_store_wait_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemAlloc);
+  }
+}
+
+}  // namespace dq
+}  // namespace ea

@@ -95,7 +95,8 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c,
              int64_t mask_head_stride_words, int kv_block,
              void* o, float* lse, void* stream);
 
-/* Bytes of device workspace attn_bwd needs for these sizes (float32 D and dQ accumulators). */
+/* Bytes of device workspace attn_bwd needs for these sizes: 16-bit types, a per-row table of
+ * float32 LSE*log2(e) and D with n rounded up to 128 rows per head; float32, per-row D. */
 size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int n, int d);
 
 /*

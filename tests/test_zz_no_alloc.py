@@ -65,11 +65,11 @@ def test_noalloc_matches_attn_bwd_on_two_calls(dtype):
 def test_noalloc_refuses_problems_larger_than_its_scratch():
     lib = ea.load()
     noalloc = _noalloc(lib)
-    need = lib.attn_bwd_workspace_bytes(2, 1, 64, 4096, 128)
+    need = lib.attn_bwd_workspace_bytes(2, 1, 128, 70000, 128)
     assert need > (32 << 20)
     buf = torch.empty(64, dtype=torch.bfloat16, device="cuda")
     p = _p(buf)
-    rc = noalloc(2, 1, 64, 4096, 128, 0.1, p, p, p, p, p, p, 0, ctypes.c_void_p(0), 0, 0, 0,
+    rc = noalloc(2, 1, 128, 70000, 128, 0.1, p, p, p, p, p, p, 0, ctypes.c_void_p(0), 0, 0, 0,
                  p, p, p, ctypes.c_void_p(0))
     assert rc == ea.ATTN_ERR_WORKSPACE
     assert "attn_bwd_noalloc" in ea.attn_last_error()
