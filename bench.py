@@ -57,7 +57,7 @@ def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith(("bwd_tc", "tile", "ptx")):
+        if name.startswith(("bwd_tc", "dq_tc", "bwd_aux", "tile", "ptx")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
@@ -65,8 +65,8 @@ def kernel_source_digest():
 
 
 def profiled_traffic():
-    """DRAM bytes per launch of the backward kernel from the committed ncu summary, or None
-    if the summary is missing or was taken from different kernel sources."""
+    """DRAM bytes per attn_bwd call (its three launches) from the committed ncu summary, or
+    None if the summary is missing or was taken from different kernel sources."""
     path = os.path.join(ROOT, "profiles", "bwd_tc_train_bf16_d128.md")
     if not os.path.exists(path):
         return None
@@ -329,8 +329,9 @@ def run_ours(args):
         "bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
         "frac": achieved / burst,
         "traffic": profiled_traffic() if dominant == "bwd" else None,
-        "kernel": ("bwd_tc_kernel<bf16, d=128>, timed as the whole attn_bwd call "
-                   "(preprocessing + main + dQ postprocessing launches)" if dominant == "bwd"
+        "kernel": ("attn_bwd, timed as the whole call: row-table preprocessing, "
+                   "bwd_tc_kernel<bf16, d=128> (dK, dV) and dq_tc_kernel<bf16, d=128> (dQ)"
+                   if dominant == "bwd"
                    else "fwd_tc_kernel<bf16, d=128, b=128>"),
         "peak_source": f"bf16_tflops burst ({kind}); kernel launches of a few ms",
         "algorithmic": f"{dom_flop:.4g} FLOP per launch = "

@@ -49,8 +49,8 @@ __global__ void __launch_bounds__(256) pre_kernel(const T* __restrict__ O, const
 
 // Row table of the tensor-core backward, padded to n_pad rows per head: L2 = LSE * log2(e)
 // (+inf for rows with no allowed key and rows past n, so that their probabilities are 0) and
-// D = rowsum(dO * O) (0 past n).  d/4 lanes cover a row with 8-byte loads (4 elements), so a
-// warp takes 32/(d/4) rows at once.
+// D = rowsum(dO * O) (0 past n).  d/8 lanes cover a row with 16-byte loads (8 elements), a warp
+// takes 32/(d/8) rows at once, and each thread keeps two such row groups in flight.
 template <typename T>
 __global__ void __launch_bounds__(256) pre_rows_kernel(const T* __restrict__ O,
                                                        const T* __restrict__ G,
@@ -58,41 +58,53 @@ __global__ void __launch_bounds__(256) pre_rows_kernel(const T* __restrict__ O,
                                                        float* __restrict__ L2,
                                                        float* __restrict__ Dv, int64_t heads, int n,
                                                        int n_pad, int d) {
-  const int lpr = d / 4;
+  constexpr int kGroups = 2;
+  const int lpr = d / 8;
   const int rpw = 32 / lpr;
   const int lane = threadIdx.x & 31;
   const int sub = lane / lpr, part = lane % lpr;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t total = heads * n_pad;
-  for (int64_t base = warp0 * rpw; base < total; base += nwarps * rpw) {
-    const int64_t rr = base + sub;
-    int64_t bh = 0, r = 0;
-    bool live = false;
-    if (rr < total) {
-      bh = rr / n_pad;
-      r = rr - bh * n_pad;
-      live = r < n;
-    }
-    float acc = 0.0f;
-    if (live) {
-      const int64_t off = (bh * n + r) * d + 4 * part;
-      const uint2 ov = *reinterpret_cast<const uint2*>(O + off);
-      const uint2 gv = *reinterpret_cast<const uint2*>(G + off);
-      const T* o4 = reinterpret_cast<const T*>(&ov);
-      const T* g4 = reinterpret_cast<const T*>(&gv);
+  for (int64_t base = warp0 * rpw; base < total; base += nwarps * rpw * kGroups) {
+    int64_t rr[kGroups], bh[kGroups], r[kGroups];
+    bool live[kGroups];
+    uint4 ov[kGroups], gv[kGroups];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc = fmaf(to_f(o4[e]), to_f(g4[e]), acc);
-    }
-    for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-    if (rr < total && part == 0) {
-      float l2 = INFINITY;
-      if (live) {
-        const float lv = lse[bh * n + r];
-        if (lv != -INFINITY) l2 = lv * 1.4426950408889634f;
+    for (int g = 0; g < kGroups; ++g) {
+      rr[g] = base + static_cast<int64_t>(g) * nwarps * rpw + sub;
+      bh[g] = 0;
+      r[g] = 0;
+      live[g] = false;
+      if (rr[g] < total) {
+        bh[g] = rr[g] / n_pad;
+        r[g] = rr[g] - bh[g] * n_pad;
+        live[g] = r[g] < n;
       }
-      L2[rr] = l2;
-      Dv[rr] = live ? acc : 0.0f;
+      ov[g] = gv[g] = make_uint4(0u, 0u, 0u, 0u);
+      if (live[g]) {
+        const int64_t off = (bh[g] * n + r[g]) * d + 8 * part;
+        ov[g] = *reinterpret_cast<const uint4*>(O + off);
+        gv[g] = *reinterpret_cast<const uint4*>(G + off);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+      const T* o8 = reinterpret_cast<const T*>(&ov[g]);
+      const T* g8 = reinterpret_cast<const T*>(&gv[g]);
+      float acc = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(to_f(o8[e]), to_f(g8[e]), acc);
+      for (int off = lpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+      if (rr[g] < total && part == 0) {
+        float l2 = INFINITY;
+        if (live[g]) {
+          const float lv = lse[bh[g] * n + r[g]];
+          if (lv != -INFINITY) l2 = lv * 1.4426950408889634f;
+        }
+        L2[rr[g]] = l2;
+        Dv[rr[g]] = live[g] ? acc : 0.0f;
+      }
     }
   }
 }
@@ -160,8 +172,8 @@ int launch_bwd_pre(int dtype, const AttnArgs& a, float* D, float* zero, size_t z
 int launch_bwd_pre_rows(bool bf16, const AttnArgs& a, float* L2, float* Dv, int n_pad,
                         cudaStream_t s, std::string& err) {
   const int64_t heads = static_cast<int64_t>(a.B) * a.H;
-  const int rpw = 32 / (a.d / 4);
-  const int grid = aux::grid_for(heads * n_pad, 8 * rpw);
+  const int rpw = 32 / (a.d / 8);
+  const int grid = aux::grid_for(heads * n_pad, 8 * rpw * 2);
   if (bf16)
     aux::pre_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.d_o), a.lse, L2,

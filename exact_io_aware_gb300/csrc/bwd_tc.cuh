@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nsteps; ++i) {
       const int s = i % NS;
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
-      if (!mbar_wait(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
+      if (!mbar_wait_spin(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars.qdo_full[s], 2 * TQ::kBytes);
 #pragma unroll
@@ -303,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);  // Sᵀ, dPᵀ
       constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);  // dV, dK
       const uint32_t sk = smem_u32(sK), sv = smem_u32(sV);
-      bool ok = mbar_wait(&bars.kv_full, 0, p.status, 22);
+      bool ok = mbar_wait_spin(&bars.kv_full, 0, p.status, 22);
       auto wait_qdo = [&](int i) -> bool {
-        return mbar_wait(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
+        return mbar_wait_spin(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
       };
       auto issue_s = [&](int i) {
         const uint32_t qb = smem_u32(sQ + (i % NS) * TQ::kBytes);
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % NS;
         const uint32_t qb = smem_u32(sQ + s * TQ::kBytes);
         const uint32_t gb = smem_u32(sG + s * TQ::kBytes);
-        ok = mbar_wait(&bars.p_full, i & 1, p.status, 24);
+        ok = mbar_wait_spin(&bars.p_full, i & 1, p.status, 24);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_s(i + 1);
         }
-        ok = mbar_wait(&bars.ds_full, i & 1, p.status, 25);
+        ok = mbar_wait_spin(&bars.ds_full, i & 1, p.status, 25);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -376,21 +376,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
       const float* L = sL + (i % NS) * BQ;
       const float* Dd = sD + (i % NS) * BQ;
-      ok = mbar_wait(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
+      ok = mbar_wait_spin(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
       if (!ok) break;
-      ok = mbar_wait(&bars.s_full, i & 1, p.status, 27);
+      ok = mbar_wait_spin(&bars.s_full, i & 1, p.status, 27);
       if (!ok) break;
       tc_fence_after();
       uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
+      // both 32-column chunks are loaded before one wait: the load latency is paid once
+      uint32_t rr[kHalf / 32][32];
+#pragma unroll
+      for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tS + c_lo + 32 * h, rr[h]);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
-        uint32_t rr[32];
-        tmem_ld32(tS + c0, rr);
-        tmem_wait_ld();
         float pv[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[k]) * sl2 - L[c0 + k]);
+        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[cc / 32][k]) * sl2 - L[c0 + k]);
         // Masking is a separate pass over the chunk so the common (full-block) path above
         // stays one compact run of instructions.
         if (partial) {
@@ -422,22 +424,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.p_full);
 
-      ok = mbar_wait(&bars.dp_full, i & 1, p.status, 28);
+      ok = mbar_wait_spin(&bars.dp_full, i & 1, p.status, 28);
       if (!ok) break;
       tc_fence_after();
+      uint32_t dp[kHalf / 32][32];
+#pragma unroll
+      for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tP + c_lo + 32 * h, dp[h]);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
-        uint32_t dp[32];
-        tmem_ld32(tP + c0, dp);
-        tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
           unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
-          const float g0 = p0 * (__uint_as_float(dp[2 * k]) - Dd[c0 + 2 * k]);
-          const float g1 = p1 * (__uint_as_float(dp[2 * k + 1]) - Dd[c0 + 2 * k + 1]);
+          const float g0 = p0 * (__uint_as_float(dp[cc / 32][2 * k]) - Dd[c0 + 2 * k]);
+          const float g1 = p1 * (__uint_as_float(dp[cc / 32][2 * k + 1]) - Dd[c0 + 2 * k + 1]);
           pk[k] = pack2<kBf16>(g0, g1);
         }
         tmem_st16(tP + packed_col(c0), pk);
@@ -450,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
     if (warp < 4) {
-      if (ok) ok = mbar_wait(&bars.kv_done, 0, p.status, 31);
+      if (ok) ok = mbar_wait_spin(&bars.kv_done, 0, p.status, 31);
       tc_fence_after();
       if (ok) {
 #pragma unroll

@@ -203,13 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % NS;
         const uint32_t ph = (i / NS) & 1;
         const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
-        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, p.status, 42)) break;
+        if (!mbar_wait_spin(&bars.k_empty[s], ph ^ 1, p.status, 42)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], TK::kBytes);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b)
           tma_load_3d(sK + s * TK::kBytes + b * TK::kBoxBytes, &tm_k, &bars.k_full[s],
                       b * TK::L::kBoxCols, key0, bh);
-        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, p.status, 41)) break;
+        if (!mbar_wait_spin(&bars.v_empty[s], ph ^ 1, p.status, 41)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], TK::kBytes);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b)
@@ -223,9 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);  // S, dP
       constexpr uint32_t id_q = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dQ
       const uint32_t qb = smem_u32(sQ), gb = smem_u32(sG);
-      bool ok = nsteps == 0 || mbar_wait(&bars.qg_full, 0, p.status, 43);
+      bool ok = nsteps == 0 || mbar_wait_spin(&bars.qg_full, 0, p.status, 43);
       auto issue_s = [&](int i) -> bool {
-        if (!mbar_wait(&bars.k_full[i % NS], (i / NS) & 1, p.status, 44)) return false;
+        if (!mbar_wait_spin(&bars.k_full[i % NS], (i / NS) & 1, p.status, 44)) return false;
         tc_fence_after();
         const uint32_t kb = smem_u32(sK + (i % NS) * TK::kBytes);
 #pragma unroll
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_dp = [&](int i) -> bool {
-        if (!mbar_wait(&bars.v_full[i % NS], (i / NS) & 1, p.status, 45)) return false;
+        if (!mbar_wait_spin(&bars.v_full[i % NS], (i / NS) & 1, p.status, 45)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(sV + (i % NS) * TK::kBytes);
 #pragma unroll
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = i + 1 < nsteps;
         if (more) ok = issue_s(i + 1);
         if (!ok) break;
-        ok = mbar_wait(&bars.ds_full, i & 1, p.status, 46);
+        ok = mbar_wait_spin(&bars.ds_full, i & 1, p.status, 46);
         if (!ok) break;
         tc_fence_after();
         const uint32_t kb = smem_u32(sK + (i % NS) * TK::kBytes);
@@ -297,20 +297,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mword[q] = w;
         }
       }
-      ok = mbar_wait(&bars.s_full[i & 1], (i >> 1) & 1, p.status, 47);
+      ok = mbar_wait_spin(&bars.s_full[i & 1], (i >> 1) & 1, p.status, 47);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tS = tmem + C::kColS + (i & 1) * BN + lane_off;
       uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
+      // both 32-column chunks are loaded before one wait: the load latency is paid once
+      uint32_t rr[kHalf / 32][32];
+#pragma unroll
+      for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tS + c_lo + 32 * h, rr[h]);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
-        uint32_t rr[32];
-        tmem_ld32(tS + c0, rr);
-        tmem_wait_ld();
         float pv[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[k]) * sl2 - lse_l2);
+        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[cc / 32][k]) * sl2 - lse_l2);
         if (partial) {
           if (p.mask_kind == kMaskBitmap) {
             const uint32_t w = mword[cc / 32];
@@ -329,22 +331,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k) pkeep[cc / 2 + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
       }
-      ok = mbar_wait(&bars.dp_full, i & 1, p.status, 48);
+      ok = mbar_wait_spin(&bars.dp_full, i & 1, p.status, 48);
       if (!ok) break;
       tc_fence_after();
+      uint32_t dp[kHalf / 32][32];
+#pragma unroll
+      for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tP + c_lo + 32 * h, dp[h]);
+      tmem_wait_ld();
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
-        uint32_t dp[32];
-        tmem_ld32(tP + c0, dp);
-        tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
           unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
-          pk[k] = pack2<kBf16>(p0 * (__uint_as_float(dp[2 * k]) - dd),
-                               p1 * (__uint_as_float(dp[2 * k + 1]) - dd));
+          pk[k] = pack2<kBf16>(p0 * (__uint_as_float(dp[cc / 32][2 * k]) - dd),
+                               p1 * (__uint_as_float(dp[cc / 32][2 * k + 1]) - dd));
         }
         tmem_st16(tP + packed_col(c0), pk);
       }
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     // dQ = c * (dS K) rounded and stored through the (now idle) Q tile.
     if (warp < 4 && row0 < n) {
-      if (ok && nsteps > 0) ok = mbar_wait(&bars.dq_done, 0, p.status, 49);
+      if (ok && nsteps > 0) ok = mbar_wait_spin(&bars.dq_done, 0, p.status, 49);
       tc_fence_after();
       if (ok) {
 #pragma unroll

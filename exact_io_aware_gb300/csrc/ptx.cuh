@@ -70,6 +70,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-suspending probe of the phase: the thread keeps polling instead of sleeping in the
+// barrier, which hands off sooner where every role waits on short, frequent phases.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Upper bound on any single wait: 2 seconds of GPU wall time.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -83,6 +96,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
+      if (device_timed_out(status) || global_ns() - t0 > kWaitLimitNs) break;
+    }
+  }
+  raise_timeout(status, site);
+  return false;
+}
+
+// mbar_wait with polling probes (mbar_test_wait); same bound and timeout reporting.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                               uint32_t site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 255u) == 0) {
       if (device_timed_out(status) || global_ns() - t0 > kWaitLimitNs) break;
     }
   }
