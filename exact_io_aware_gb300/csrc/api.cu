@@ -31,6 +31,10 @@ int status_ptr(uint32_t** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_UNSUPPORTED, "device ordinal too large");
+  // Bind the device's primary context to the calling thread: the tensor-map encoder is a driver
+  // call and fails on a thread (an autograd worker, say) whose first CUDA call it would be.
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
   if (!g_status_ptr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_status_word);

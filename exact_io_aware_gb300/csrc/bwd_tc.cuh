@@ -51,12 +51,16 @@ struct BwdParams {
   const uint32_t* mask_bits;
   int64_t mask_row_words;
   int64_t mask_head_stride_words;
-  // Row table [heads][n_pad] (n_pad = n rounded up to 128), written by the preprocessing
-  // step: L2 = LSE * log2(e), +inf where a row has no allowed key or lies past n; Dv = D_i,
-  // 0 past n.
-  const float* L2;
-  const float* Dv;
+  // Row table [heads][n_pad] (n_pad = n rounded up to 128), written by the dQ kernel, which
+  // runs first, and read by the dK/dV kernel: L2 = LSE * log2(e), +inf where a row has no
+  // allowed key or lies past n; Dv = D_i = rowsum(dO_i * O_i), 0 past n.
+  float* L2;
+  float* Dv;
   int n_pad;
+  // inputs the dQ kernel builds the table from
+  const float* lse;
+  const void* o;
+  const void* d_o;
   uint32_t* status;
 };
 
@@ -245,8 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
-    // Lane 0 issues the TMA loads; all lanes stage each block's LSE (log2 units, +inf for
-    // rows past n or with an empty allowed set), D and, for bitmap masks, allowed-key words.
+    // Lane 0 issues the TMA loads, including the bulk copies of each block's rows of the row
+    // table; for bitmap masks all lanes stage the block's allowed-key words.
     const float* l2_h = p.L2 + static_cast<int64_t>(bh) * p.n_pad;
     const float* d_h = p.Dv + static_cast<int64_t>(bh) * p.n_pad;
     if (lane == 0) {

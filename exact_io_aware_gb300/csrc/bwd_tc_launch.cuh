@@ -11,7 +11,7 @@ namespace bwd {
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 
 template <bool kBf16, int D>
-int run(const AttnArgs& a, const float* L2, cudaStream_t s, std::string& err) {
+int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   using Cfg = Config<D>;
   using QCfg = dq::Config<D>;
   const bool bitmap = a.mask_kind == kMaskBitmap;
@@ -35,22 +35,13 @@ int run(const AttnArgs& a, const float* L2, cudaStream_t s, std::string& err) {
     return -5;
   }
   const int n_pad = bwd_pad_rows(a.n);
+  float* L2 = table;
   BwdParams p{a.n,  a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
-              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.status};
+              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.status};
   const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
-  auto kern = bwd_tc_kernel<kBf16, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e == cudaSuccess) {
-    kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, tg, tdk, tdv, p);
-    e = cudaGetLastError();
-  }
-  if (e != cudaSuccess) {
-    err = std::string("dK/dV launch: ") + cudaGetErrorString(e);
-    return -5;
-  }
+  // the dQ kernel writes the row table the dK/dV kernel reads
   auto qkern = dq::dq_tc_kernel<kBf16, D>;
-  e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(qsmem));
   if (e == cudaSuccess) {
     qkern<<<grid, dq::kThreads, qsmem, s>>>(tq, tk, tv, tg, tdq, p);
@@ -58,6 +49,17 @@ int run(const AttnArgs& a, const float* L2, cudaStream_t s, std::string& err) {
   }
   if (e != cudaSuccess) {
     err = std::string("dQ launch: ") + cudaGetErrorString(e);
+    return -5;
+  }
+  auto kern = bwd_tc_kernel<kBf16, D>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e == cudaSuccess) {
+    kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, tg, tdk, tdv, p);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    err = std::string("dK/dV launch: ") + cudaGetErrorString(e);
     return -5;
   }
   return 0;

@@ -7,7 +7,10 @@
 // (dK and dV come from the key-tile kernel in bwd_tc.cuh, which recomputes the same p and g.)
 //
 // One CTA owns a tile of 128 query rows of one head and walks the 128-key blocks they reach,
-// exactly like the forward; LSE_i and D_i are per-row scalars held by the row's thread.
+// exactly like the forward; LSE_i and D_i are per-row scalars held by the row's thread.  The
+// kernel computes D_i = rowsum(dO_i * O_i) itself (each softmax warp of a row sums half of
+// the columns) and writes the row table (LSE_i log2 e and D_i) that the dK/dV kernel, launched
+// after it, copies per query block.
 // Per key block j:
 //   S  = Q K_jᵀ           (tensor memory, one query row per lane; two buffers)
 //   P  = exp2(S c log2e - LSE log2e)     softmax warps, kept in registers
@@ -24,6 +27,8 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "bwd_tc.cuh"
 
@@ -78,6 +83,7 @@ struct Barriers {
   uint64_t dq_done;
   uint32_t tmem_base;
   uint32_t nsteps;
+  float dpart[2][kRows];  // per-row partial sums of dO * O over each half of the columns
 };
 
 template <bool kBf16, int D>
@@ -273,9 +279,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kHalf = BN / 2;  // key columns of this warp: [c_lo, c_lo + kHalf)
     const int c_lo = (warp / 4) * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
+    // D_i: this warp sums dO * O over its half of the head dimension (16-byte loads)
+    const int half = warp / 4;
+    float dpar = 0.0f;
+    if (row < n) {
+      using E = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
+      const int64_t off = (static_cast<int64_t>(bh) * n + row) * D + half * (D / 2);
+      const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.o) + off);
+      const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.d_o) + off);
+#pragma unroll
+      for (int v = 0; v < D / 16; ++v) {
+        const uint4 a = __ldg(o4 + v), g = __ldg(g4 + v);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float a0, a1, g0, g1;
+          unpack2<kBf16>(aw[e], a0, a1);
+          unpack2<kBf16>(gw[e], g0, g1);
+          dpar = fmaf(a0, g0, dpar);
+          dpar = fmaf(a1, g1, dpar);
+        }
+      }
+    }
+    bars.dpart[half][r] = dpar;
+    bwd::named_barrier(3, kSoftmaxWarps * 32);
+    const float dd = row < n ? bars.dpart[0][r] + bars.dpart[1][r] : 0.0f;
     // rows past n or with no allowed key carry +inf here, so their probabilities are 0
-    const float lse_l2 = __ldg(p.L2 + static_cast<int64_t>(bh) * p.n_pad + row);
-    const float dd = __ldg(p.Dv + static_cast<int64_t>(bh) * p.n_pad + row);
+    float lse_l2 = INFINITY;
+    if (row < n) {
+      const float lv = __ldg(p.lse + static_cast<int64_t>(bh) * n + row);
+      if (lv != -INFINITY) lse_l2 = lv * 1.4426950408889634f;
+    }
+    if (half == 0) {  // this tile's rows of the table, padded rows included
+      p.L2[static_cast<int64_t>(bh) * p.n_pad + row] = lse_l2;
+      p.Dv[static_cast<int64_t>(bh) * p.n_pad + row] = dd;
+    }
     const uint32_t* rowbits =
         p.mask_kind == kMaskBitmap
             ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +

@@ -52,20 +52,10 @@ int launch_bwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err
 int launch_fwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
 int launch_bwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
 
-// D_i = sum_a dO[i][a] * O[i][a] (float32) for 16-bit or float32 inputs; optionally zeroes a
-// float32 accumulator of `zero_elems` elements.
-int launch_bwd_pre(int dtype, const AttnArgs& a, float* D, float* zero, size_t zero_elems,
-                   cudaStream_t s, std::string& err);
+// D_i = sum_a dO[i][a] * O[i][a] for float32 inputs.
+int launch_bwd_pre_f32(const AttnArgs& a, float* D, cudaStream_t s, std::string& err);
 // Rows per head of the tensor-core backward's row table: n rounded up to 128.
 constexpr int bwd_pad_rows(int n) { return (n + 127) / 128 * 128; }
-
-// Row table of the tensor-core backward: L2 = LSE*log2(e) (+inf for empty rows and rows past
-// n) and D, each [B*H][n_pad] float32, for 16-bit O and dO.
-int launch_bwd_pre_rows(bool bf16, const AttnArgs& a, float* L2, float* Dv, int n_pad,
-                        cudaStream_t s, std::string& err);
-// dQ = c * acc, rounded to the 16-bit output type.
-int launch_bwd_post(bool bf16, const AttnArgs& a, const float* acc, cudaStream_t s,
-                    std::string& err);
 
 size_t bwd_tc_workspace_bytes(int B, int H, int n, int d);
 size_t bwd_f32_workspace_bytes(int B, int H, int n, int d);

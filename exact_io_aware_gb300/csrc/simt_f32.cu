@@ -431,7 +431,7 @@ size_t bwd_f32_workspace_bytes(int B, int H, int n, int) {
 
 int launch_bwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err) {
   float* Dv = static_cast<float*>(a.workspace);
-  if (int rc = launch_bwd_pre(0, a, Dv, nullptr, 0, s, err)) return rc;
+  if (int rc = launch_bwd_pre_f32(a, Dv, s, err)) return rc;
   int rc;
   switch (a.d) {
     case 16: rc = f32::bwd_d<16>(a, Dv, s, err); break;
