@@ -57,24 +57,25 @@ def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith(("bwd_tc", "dq_tc", "bwd_aux", "tile", "ptx")):
+        if name.startswith(("bwd_tc", "dq_tc", "tile", "ptx")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per attn_bwd call (its three launches) from the committed ncu summary, or
+def profiled_traffic(path=None):
+    """DRAM bytes per attn_bwd call (its two launches) from the committed ncu summary, or
     None if the summary is missing or was taken from different kernel sources."""
-    path = os.path.join(ROOT, "profiles", "bwd_tc_train_bf16_d128.md")
+    path = path or os.path.join(ROOT, "profiles", "bwd_tc_train_bf16_d128.md")
     if not os.path.exists(path):
         return None
     vals = {}
     with open(path) as f:
         for line in f:
-            if "=" in line and line.strip().startswith(("dram_bytes_per_launch", "source_digest")):
-                k, v = line.strip().strip("`").split("=", 1)
+            text = line.strip().strip("`")
+            if "=" in text and text.startswith(("dram_bytes_per_launch", "source_digest")):
+                k, v = text.split("=", 1)
                 vals[k.strip()] = v.strip().strip("`")
     if vals.get("source_digest") != kernel_source_digest():
         return None
@@ -329,8 +330,8 @@ def run_ours(args):
         "bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
         "frac": achieved / burst,
         "traffic": profiled_traffic() if dominant == "bwd" else None,
-        "kernel": ("attn_bwd, timed as the whole call: row-table preprocessing, "
-                   "bwd_tc_kernel<bf16, d=128> (dK, dV) and dq_tc_kernel<bf16, d=128> (dQ)"
+        "kernel": ("attn_bwd, timed as the whole call: dq_tc_kernel<bf16, d=128> (dQ and "
+                   "the row table of LSE and D) then bwd_tc_kernel<bf16, d=128> (dK, dV)"
                    if dominant == "bwd"
                    else "fwd_tc_kernel<bf16, d=128, b=128>"),
         "peak_source": f"bf16_tflops burst ({kind}); kernel launches of a few ms",
@@ -356,7 +357,7 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 3 * args.steps,  # attn_fwd: 1 launch; attn_bwd: 2
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
