@@ -311,7 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + 2 * BN + t * D;
     const bool active = (act >> t) & 1u;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const float sl2 = p.c * 1.4426950408889634f;
+    // The scale c·log2(e) is folded into the exponent's FFMA, so the raw scores are reduced:
+    // their maximum for c > 0, their minimum for c < 0; c = 0 is run as the smallest normal
+    // positive scale, which leaves every finite score's exponent at zero (all weights equal).
+    const float sl2_raw = p.c * 1.4426950408889634f;
+    const float sl2 = sl2_raw == 0.0f ? 1.17549435e-38f : sl2_raw;
+    const bool pos = sl2 > 0.0f;
+    const float mv = pos ? -INFINITY : INFINITY;  // raw value of a masked score
     float m = -INFINITY;  // running maximum, log2 units (possibly stale by < kLazy)
     float l = 0.0f;       // running normaliser relative to m
     uint32_t s_phase = 0;
@@ -330,6 +336,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       s_phase ^= 1;
       tc_fence_after();
+      // Masking (partial blocks only), done in tensor memory before the scores are read: each
+      // 32-key chunk is loaded, its masked entries set to the raw value whose scaled image is
+      // -inf, and stored back.  A rolled loop keeps this rare path small, so the common path
+      // below stays one compact run of instructions.
+      if (__builtin_expect(cls == kPartial, 0)) {
+#pragma unroll 1
+        for (int q = 0; q < BN / 32; ++q) {
+          const int kq = key0 + q * 32;
+          uint32_t w;
+          if (p.mask_kind == kMaskBitmap) {
+            w = (row < n && kq < n) ? __ldg(rowbits + kq / 32) : 0u;
+            const int nk = n - kq;
+            if (nk < 32) w &= nk > 0 ? (1u << nk) - 1u : 0u;
+          } else {
+            // allowed keys kq .. lim: lim = min(row, n - 1) (causal) or n - 1 (key tail)
+            const int lim = p.mask_kind == kMaskCausal ? min(row, n - 1) : n - 1;
+            const int cnt = min(max(lim - kq + 1, 0), 32);
+            w = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
+          }
+          uint32_t rr[32];
+          tmem_ld32(tS + lane_off + q * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (!((w >> k) & 1u)) rr[k] = __float_as_uint(mv);
+          tmem_st16(tS + lane_off + q * 32, *reinterpret_cast<const uint32_t(*)[16]>(rr));
+          tmem_st16(tS + lane_off + q * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(rr + 16));
+        }
+        tmem_wait_st();
+      }
       // All TMEM loads first, one wait: the row's BN raw scores land in registers.
       float sv[BN];
       {
@@ -341,44 +377,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < BN; ++k) sv[k] = __uint_as_float(rr[k]);
       }
-      // With c > 0 the scale is folded into the exponent's FFMA and the maximum is taken on
-      // raw scores; otherwise (c <= 0) the scores are scaled first.
-      const bool fold = sl2 > 0.0f;
-      if (!fold) {
+      // Row extreme of the raw scores with four independent accumulators (short chains).
+      float a0 = mv, a1 = mv, a2 = mv, a3 = mv;
+      if (pos) {
 #pragma unroll
-        for (int k = 0; k < BN; ++k) sv[k] *= sl2;
-      }
-      if (cls == kPartial) {
-        if (p.mask_kind == kMaskCausal) {
-#pragma unroll
-          for (int k = 0; k < BN; ++k)
-            if (key0 + k > row || key0 + k >= n) sv[k] = -INFINITY;
-        } else if (p.mask_kind == kMaskBitmap) {
-#pragma unroll
-          for (int q = 0; q < BN / 32; ++q) {
-            const int kq = key0 + q * 32;
-            uint32_t w = (row < n && kq < n) ? __ldg(rowbits + kq / 32) : 0u;
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-              if (!((w >> k) & 1u) || kq + k >= n) sv[q * 32 + k] = -INFINITY;
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < BN; ++k)
-            if (key0 + k >= n) sv[k] = -INFINITY;
+        for (int k = 0; k < BN; k += 8) {
+          a0 = fmax3(a0, sv[k], sv[k + 1]);
+          a1 = fmax3(a1, sv[k + 2], sv[k + 3]);
+          a2 = fmax3(a2, sv[k + 4], sv[k + 5]);
+          a3 = fmax3(a3, sv[k + 6], sv[k + 7]);
         }
-      }
-      // Row maximum with four independent accumulators (short dependency chains).
-      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+        a0 = fmax3(a0, a1, fmaxf(a2, a3));
+      } else {
 #pragma unroll
-      for (int k = 0; k < BN; k += 8) {
-        a0 = fmax3(a0, sv[k], sv[k + 1]);
-        a1 = fmax3(a1, sv[k + 2], sv[k + 3]);
-        a2 = fmax3(a2, sv[k + 4], sv[k + 5]);
-        a3 = fmax3(a3, sv[k + 6], sv[k + 7]);
+        for (int k = 0; k < BN; k += 8) {
+          a0 = fmin3(a0, sv[k], sv[k + 1]);
+          a1 = fmin3(a1, sv[k + 2], sv[k + 3]);
+          a2 = fmin3(a2, sv[k + 4], sv[k + 5]);
+          a3 = fmin3(a3, sv[k + 6], sv[k + 7]);
+        }
+        a0 = fmin3(a0, a1, fminf(a2, a3));
       }
-      float mx = fmax3(a0, a1, fmaxf(a2, a3));
-      if (fold && mx != -INFINITY) mx *= sl2;
+      const float mx = a0 == mv ? -INFINITY : a0 * sl2;  // block maximum, log2 units
       float alpha = 1.0f;
       if (mx > m + kLazy || (m == -INFINITY && mx != -INFINITY)) {
         alpha = ex2(m - mx);  // m = -inf gives 0
@@ -386,10 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       const float neg_mu = (m == -INFINITY) ? 0.0f : -m;
-      const float sc = fold ? sl2 : 1.0f;
-      // z *= alpha: only after the first block, and only if some row of this warp needs it.
-      if (!first && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-#pragma unroll
+      const float sc = sl2;
+      // z *= alpha: only after the first block, and only if some row of this warp needs it
+      // (rare with the lazy threshold, so the loop stays rolled and out of the common path).
+      if (__builtin_expect(!first && __any_sync(0xFFFFFFFFu, alpha != 1.0f), 0)) {
+#pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 16) {
           uint32_t rr[16];
           tmem_ld16(tO + lane_off + c0, rr);

@@ -319,6 +319,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// min(a, b, c) in one instruction.
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // Pack two floats into one 32-bit word of 16-bit values: `lo` in bits 0-15, `hi` in 16-31.
 template <bool kBf16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
