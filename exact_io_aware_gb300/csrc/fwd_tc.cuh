@@ -6,14 +6,21 @@
 // and at the end O_i = z_i / l_i.  Retained statistic: LSE_i = m_i + ln l_i.
 //
 // One CTA owns two tiles of 128 query rows of one head (256 rows).  Roles:
-//   warps 0-3  softmax for tile 0   (thread = query row = TMEM lane)
-//   warps 4-7  softmax for tile 1
-//   warp  8    TMA producer: Q tiles once, then K and V blocks through an NS-stage ring
-//   warp  9    TMEM allocator and MMA issuer (one elected thread)
+//   warp  0    MMA issuer for tile 0 (one elected lane); allocates tensor memory
+//   warp  1    MMA issuer for tile 1
+//   warps 2-5  softmax for tile 0   (thread = query row = TMEM lane of the warp's quadrant)
+//   warps 6-9  softmax for tile 1
+//   warp  10   TMA producer: Q tiles once, then K and V blocks through two rings (NSK and
+//              NSV stages); K runs one block ahead of V, and blocks kPrefetch steps ahead are
+//              requested into L2 so that the ring loads find them there
 // Tensor memory: S_t = Q_t K_jᵀ (BN fp32 columns per tile; the 16-bit P_t is written over
 // the first BN/2 of them) and O_t, the unnormalised weighted value sum z (D columns per tile).
-// The MMA thread issues, per key block, PV_{j-1}(t0), S_j(t0), PV_{j-1}(t1), S_j(t1), so the
-// tensor core works on one tile while the other tile's softmax runs.
+// Each tile's MMA warp issues, per key block j, PV_{j-1} then S_j for its tile, so the tensor
+// core works on one tile while the other tile's softmax runs.  One issuer per tile keeps a
+// tile's waits (its softmax, the next K block) off the other tile's issue path: the tensor
+// core accepts only a few MMAs ahead, so an issuer spends most of its time blocked in issue.
+// The issuers have the lowest warp slots, which the warp schedulers favour over the
+// softmax warps they share a sub-partition with.
 //
 // Online softmax (the running-maximum recurrence of "The Arithmetic of Intelligence",
 // chapter 12): scores are taken to base 2 with the folded factor c·log2(e) (the exp2
@@ -33,24 +40,31 @@ namespace ea {
 namespace fwd {
 
 constexpr int kRowsPerTile = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kFirstSoftmaxWarp = 2;
+constexpr int kProducerWarp = 10;
 constexpr float kLazy = 8.0f;  // log2 units
 constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
+
+// Opt-in dynamic shared memory per CTA on sm_103a (227 KiB) less the kernel's static barrier
+// block.
+constexpr int kMaxDynSmem = 227 * 1024 - 1024;
+// Key blocks requested into L2 ahead of the ring loads.
+constexpr int kPrefetch = 4;
 
 template <int D, int BN>
 struct Config {
   using TQ = Tile<kRowsPerTile, D>;
   using TKV = Tile<BN, D>;
-  static constexpr int kSmemBudget = 227 * 1024 - 1024 - 512;  // minus alignment slack, barriers
-  static constexpr int kStageBytes = 2 * TKV::kBytes;          // one K block + one V block
+  static constexpr int kSmemBudget = kMaxDynSmem - 1024;  // minus the 1024-byte alignment slack
   static constexpr int kFixed = 2 * TQ::kBytes;
-  static constexpr int kMaxStepBytes = 16 * 1024;
-  static constexpr int kStagesFit = (kSmemBudget - kFixed - kMaxStepBytes) / kStageBytes;
-  static constexpr int NS = kStagesFit > 4 ? 4 : kStagesFit;
-  static_assert(NS >= 2, "need at least two pipeline stages");
+  static constexpr int kStepReserve = 1024;  // smallest step table kept room for (bitmap masks)
+  static constexpr int kSlots = (kSmemBudget - kFixed - kStepReserve) / TKV::kBytes;
+  // V is consumed one step after K, so K takes the odd slot: its loads are the ones a step waits on.
+  static constexpr int NSV = kSlots / 2 > 4 ? 4 : kSlots / 2;
+  static constexpr int NSK = kSlots - NSV > 4 ? 4 : kSlots - NSV;
+  static_assert(NSV >= 2 && NSK >= 2, "need at least two pipeline stages");
   static constexpr int kTmemCols = 2 * BN + 2 * D;
   static constexpr int kTmemAlloc = kTmemCols <= 32    ? 32
                                     : kTmemCols <= 64  ? 64
@@ -61,11 +75,13 @@ struct Config {
   // dynamic shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + 2 * TQ::kBytes;
-  static constexpr int kOffV = kOffK + NS * TKV::kBytes;
-  static constexpr int kOffSteps = kOffV + NS * TKV::kBytes;
-  static size_t smem_bytes(int n) {
-    const int nblk = (n + BN - 1) / BN;
-    return 1024 + kOffSteps + 4 * static_cast<size_t>(nblk) + 512;
+  static constexpr int kOffV = kOffK + NSK * TKV::kBytes;
+  static constexpr int kOffSteps = kOffV + NSV * TKV::kBytes;
+  // Only a bitmap mask needs the step table (one word per key block); the walk under the
+  // other masks is computed on the fly.
+  static size_t smem_bytes(int n, int mask_kind) {
+    const size_t nblk = (static_cast<size_t>(n) + BN - 1) / BN;
+    return 1024 + kOffSteps + (mask_kind == kMaskBitmap ? 4 * nblk : 0);
   }
 };
 
@@ -77,6 +93,7 @@ struct Barriers {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint32_t tmem_base;
   uint32_t nsteps;
+  uint32_t act;  // bit t: tile t takes part in some step
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -87,6 +104,27 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Step word of the walk under no mask or the causal mask: key block j, and for each of the two
+// query tiles (rows r0 .. r0 + 127 of the pair) whether it skips the block, takes it whole or
+// needs the mask pass (causal diagonal or the ragged key tail).  Same encoding as the bitmap
+// table: j | cls0 << 16 | cls1 << 18.
+__device__ __forceinline__ uint32_t dense_step(int j, int BN, int nblk, int n, int pair_row0,
+                                               bool causal) {
+  uint32_t w = static_cast<uint32_t>(j);
+  const bool tail_blk = (n % BN) != 0 && j == nblk - 1;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = pair_row0 + t * kRowsPerTile;
+    if (r0 >= n) continue;
+    const int last_row = min(r0 + kRowsPerTile, n) - 1;
+    const bool any = !causal || j * BN <= last_row;
+    const bool all = !causal || (j + 1) * BN - 1 <= r0;
+    const uint32_t cls = any ? ((all && !tail_blk) ? kFull : kPartial) : kSkip;
+    w |= cls << (16 + 2 * t);
+  }
+  return w;
+}
+
 template <bool kBf16, int D, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -95,7 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Config<D, BN>;
   using TQ = typename C::TQ;
   using TKV = typename C::TKV;
-  constexpr int NS = C::NS;
+  constexpr int NSK = C::NSK;
+  constexpr int NSV = C::NSV;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -122,21 +161,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.p_full[t], 4);
       mbar_init(&bars.o_done[t], 1);
     }
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars.k_full[s], 1);
-      mbar_init(&bars.k_empty[s], 1);
-      mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.v_empty[s], 1);
-    }
-    fence_barrier_init();
+    for (int s = 0; s < NSK; ++s) mbar_init(&bars.k_full[s], 1);
+    for (int s = 0; s < NSV; ++s) mbar_init(&bars.v_full[s], 1);
   }
-  if (warp == kMmaWarp) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
+  if (warp == 0) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
 
-  // Classify every key block for both tiles: skip / full / partial (mask needed).
-  for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
-  __syncthreads();
-  const bool tail = (n % BN) != 0;
-  if (p.mask_kind == kMaskBitmap) {
+  // Walk over key blocks.  Under a bitmap mask every block is classified for both tiles (skip /
+  // full / partial) into a table of the blocks some tile takes; otherwise step i is block i,
+  // up to the last block the pair's rows reach.
+  const bool use_table = p.mask_kind == kMaskBitmap;
+  const bool causal = p.mask_kind == kMaskCausal;
+  if (use_table) {
+    for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
+    __syncthreads();
     if (tid < kSoftmaxThreads) {
       const int t = tid / kRowsPerTile;
       const int row = pair_row0 + t * kRowsPerTile + (tid % kRowsPerTile);
@@ -168,43 +205,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    for (int j = tid; j < nblk; j += kThreads) {
-      uint32_t bits = 0;
-      for (int t = 0; t < 2; ++t) {
-        const int r0 = pair_row0 + t * kRowsPerTile;
-        const int last_row = min(r0 + kRowsPerTile, n) - 1;
-        if (r0 >= n) continue;
-        bool any = true, all = true;
-        if (p.mask_kind == kMaskCausal) {
-          any = j * BN <= last_row;
-          all = (j + 1) * BN - 1 <= r0;
-        }
-        if (any) bits |= (1u << t) | (all ? 0u : (4u << t));
+    __syncthreads();
+    if (tid == 0) {
+      const bool tail = (n % BN) != 0;
+      int ns = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const uint32_t b = steps[j];
+        const bool part_tail = tail && j == nblk - 1;
+        uint32_t cls0 = (b & 1u) ? (((b & 4u) || part_tail) ? kPartial : kFull) : kSkip;
+        uint32_t cls1 = (b & 2u) ? (((b & 8u) || part_tail) ? kPartial : kFull) : kSkip;
+        if (cls0 | cls1) steps[ns++] = static_cast<uint32_t>(j) | (cls0 << 16) | (cls1 << 18);
       }
-      steps[j] = bits;
+      uint32_t act = 0;
+      for (int i = 0; i < ns; ++i)
+        act |= ((steps[i] >> 16) & 3u ? 1u : 0u) | ((steps[i] >> 18) & 3u ? 2u : 0u);
+      bars.nsteps = ns;
+      bars.act = act;
     }
+  } else if (tid == 0) {
+    const int last = min(pair_row0 + 2 * kRowsPerTile, n) - 1;  // last row of the pair
+    bars.nsteps = causal ? last / BN + 1 : nblk;
+    // every tile with rows takes block 0
+    bars.act = (pair_row0 < n ? 1u : 0u) | (pair_row0 + kRowsPerTile < n ? 2u : 0u);
   }
-  __syncthreads();
   if (tid == 0) {
-    int ns = 0;
-    for (int j = 0; j < nblk; ++j) {
-      const uint32_t b = steps[j];
-      const bool part_tail = tail && j == nblk - 1;
-      uint32_t cls0 = (b & 1u) ? (((b & 4u) || part_tail) ? kPartial : kFull) : kSkip;
-      uint32_t cls1 = (b & 2u) ? (((b & 8u) || part_tail) ? kPartial : kFull) : kSkip;
-      if (cls0 | cls1) steps[ns++] = static_cast<uint32_t>(j) | (cls0 << 16) | (cls1 << 18);
-    }
-    bars.nsteps = ns;
+    // A ring stage is free once the MMA warp of every active tile has released it.
+    const uint32_t a = bars.act;
+    const uint32_t issuers = (a & 1u) + ((a >> 1) & 1u);
+    for (int s = 0; s < NSK; ++s) mbar_init(&bars.k_empty[s], issuers ? issuers : 1u);
+    for (int s = 0; s < NSV; ++s) mbar_init(&bars.v_empty[s], issuers ? issuers : 1u);
+    fence_barrier_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const int nsteps = bars.nsteps;
   const uint32_t tmem = bars.tmem_base;
+  const uint32_t act = bars.act;
   // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*D
-  uint32_t act = 0;  // bit t: tile t takes part in some step
-  for (int i = 0; i < nsteps; ++i) act |= ((steps[i] >> 16) & 3u ? 1u : 0u) | ((steps[i] >> 18) & 3u ? 2u : 0u);
+  auto step_at = [&](int i) -> uint32_t {
+    return use_table ? steps[i] : dense_step(i, BN, nblk, n, pair_row0, causal);
+  };
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA producer
@@ -221,90 +262,119 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + t * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.q_full[t],
                       b * TQ::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
       }
-      for (int i = 0; i < nsteps; ++i) {
-        const int s = i % NS;
-        const uint32_t ph = (i / NS) & 1;
-        const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
-        if (!mbar_wait(&bars.k_empty[s], ph ^ 1, p.status, 1)) break;
+      // Ring loads in the order K_0, K_1, V_0, K_2, V_1, ...: K, which the next step waits
+      // on first, stays one block ahead of V.
+      auto key0_at = [&](int i) { return static_cast<int>(step_at(i) & 0xFFFFu) * BN; };
+      auto load_k = [&](int i) -> bool {
+        const int s = i % NSK;
+        if (!mbar_wait(&bars.k_empty[s], ((i / NSK) & 1) ^ 1, p.status, 1)) return false;
+        const int key0 = key0_at(i);
         mbar_arrive_expect_tx(&bars.k_full[s], TKV::kBytes);
 #pragma unroll
         for (int b = 0; b < TKV::L::kBoxes; ++b)
           tma_load_3d(sK + s * TKV::kBytes + b * TKV::kBoxBytes, &tm_k, &bars.k_full[s],
                       b * TKV::L::kBoxCols, key0, bh);
-        if (!mbar_wait(&bars.v_empty[s], ph ^ 1, p.status, 2)) break;
+        if (i + kPrefetch < nsteps) {
+          const int kp = key0_at(i + kPrefetch);
+#pragma unroll
+          for (int b = 0; b < TKV::L::kBoxes; ++b) {
+            tma_prefetch_l2_3d(&tm_k, b * TKV::L::kBoxCols, kp, bh);
+            tma_prefetch_l2_3d(&tm_v, b * TKV::L::kBoxCols, kp, bh);
+          }
+        }
+        return true;
+      };
+      auto load_v = [&](int i) -> bool {
+        const int s = i % NSV;
+        if (!mbar_wait(&bars.v_empty[s], ((i / NSV) & 1) ^ 1, p.status, 2)) return false;
+        const int key0 = key0_at(i);
         mbar_arrive_expect_tx(&bars.v_full[s], TKV::kBytes);
 #pragma unroll
         for (int b = 0; b < TKV::L::kBoxes; ++b)
           tma_load_3d(sV + s * TKV::kBytes + b * TKV::kBoxBytes, &tm_v, &bars.v_full[s],
                       b * TKV::L::kBoxCols, key0, bh);
+        return true;
+      };
+      if (nsteps > 0 && load_k(0)) {
+        for (int i = 0; i < nsteps; ++i) {
+          if (i + 1 < nsteps && !load_k(i + 1)) break;
+          if (!load_v(i)) break;
+        }
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
-    // Per step i: wait K_i; for each tile, first the PV of its previous step (if it took
-    // part), then S_i if it takes part.  Every PV is issued in the step right after its S, so
-    // each V stage is released one step after it was filled.
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);
-      constexpr uint32_t id_o = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);
-      bool ok = true;
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if (ok && ((act >> t) & 1u)) ok = mbar_wait(&bars.q_full[t], 0, p.status, 3);
-      uint32_t pend = 0;     // bit t: tile t took part in the previous step (PV owed)
-      uint32_t started = 0;  // bit t: O_t already holds a partial sum
-      uint32_t pph = 0;      // bit t: parity of the next p_full[t] phase
-      for (int i = 0; i <= nsteps && ok; ++i) {
-        const int prev = i - 1;
-        if (pend) {
-          ok = mbar_wait(&bars.v_full[prev % NS], (prev / NS) & 1, p.status, 5);
-          if (!ok) break;
-        }
-        const uint32_t cur = i < nsteps ? steps[i] : 0u;
-        const int s = i % NS;
-        if (i < nsteps) {
-          ok = mbar_wait(&bars.k_full[s], (i / NS) & 1, p.status, 6);
-          if (!ok) break;
-        }
-        tc_fence_after();
-        const uint32_t kbase = smem_u32(sK + s * TKV::kBytes);
-        const uint32_t vbase = smem_u32(sV + (prev >= 0 ? prev % NS : 0) * TKV::kBytes);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (ok && ((pend >> t) & 1u)) {
-            ok = mbar_wait(&bars.p_full[t], (pph >> t) & 1u, p.status, 4);
-            if (ok) {
-              pph ^= 1u << t;
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk)
-                mma_ts(tmem + 2 * BN + t * D, tmem + t * BN + kk * 8, TKV::desc_mn(vbase, kk),
-                       id_o, (((started >> t) & 1u) || kk > 0) ? 1u : 0u);
-              started |= 1u << t;
-            }
-          }
-          if (ok && ((cur >> (16 + 2 * t)) & 3u)) {
-            const uint32_t qbase = smem_u32(sQ + t * TQ::kBytes);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(tmem + t * BN, TQ::desc_k(qbase, kk), TKV::desc_k(kbase, kk), id_s,
-                     kk > 0 ? 1u : 0u);
-            mma_commit(&bars.s_full[t]);
-          }
-        }
+  } else if (warp < kFirstSoftmaxWarp) {
+    // ---------------------------------------------------------------- MMA issuer (tile t)
+    // Per step i: PV_{i-1} (once this tile's P_{i-1} is in tensor memory), then S_i if the tile
+    // takes block i.  PV_{i-1} reads P_{i-1} before S_i overwrites it (one thread's MMAs run in
+    // issue order).  Every step releases its K stage and the previous step's V stage, whether
+    // or not this tile used them, after waiting for the loads (which keeps each release in the
+    // stage's current phase).  The whole warp runs the loop so that descriptors stay
+    // warp-uniform; one elected lane issues.  Operand descriptors are built once per buffer: a
+    // 16-element step or a ring stage only adds a constant to the start-address field.
+    const int t = warp;
+    constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);
+    constexpr uint32_t id_o = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);
+    constexpr uint64_t kStage = TKV::kBytes >> 4;
+    const uint64_t dq = TQ::desc_k(smem_u32(sQ + t * TQ::kBytes), 0);
+    const uint64_t dk0 = TKV::desc_k(smem_u32(sK), 0);
+    const uint64_t dv0 = TKV::desc_mn(smem_u32(sV), 0);
+    const uint32_t tS = tmem + t * BN;
+    const uint32_t tO = tmem + 2 * BN + t * D;
+    bool ok = (act >> t) & 1u;
+    if (ok) ok = mbar_wait_warp(&bars.q_full[t], 0, p.status, 3);
+    bool pend = false;     // this tile took part in the previous step (PV owed)
+    bool started = false;  // O_t already holds a partial sum
+    uint32_t pph = 0;      // parity of the next p_full[t] phase
+    for (int i = 0; i <= nsteps && ok; ++i) {
+      const int prev = i - 1;
+      if (prev >= 0) {
+        ok = mbar_wait_warp(&bars.v_full[prev % NSV], (prev / NSV) & 1, p.status, 5);
         if (!ok) break;
-        if (i < nsteps) mma_commit(&bars.k_empty[s]);
-        if (pend) mma_commit(&bars.v_empty[prev % NS]);
-        pend = (((cur >> 16) & 3u) ? 1u : 0u) | (((cur >> 18) & 3u) ? 2u : 0u);
       }
+      const bool cur = i < nsteps && ((step_at(i) >> (16 + 2 * t)) & 3u) != 0;
+      const int s = i % NSK;
+      if (i < nsteps) {
+        ok = mbar_wait_warp(&bars.k_full[s], (i / NSK) & 1, p.status, 6);
+        if (!ok) break;
+      }
+      tc_fence_after();
+      if (pend) {
+        ok = mbar_wait_warp(&bars.p_full[t], pph, p.status, 4);
+        if (!ok) break;
+        pph ^= 1u;
+        tc_fence_after();
+        const uint64_t dv = dv0 + static_cast<uint64_t>(prev % NSV) * kStage;
+        if (elect_one()) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t)
-        if ((act >> t) & 1u) mma_commit(&bars.o_done[t]);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tO, tS + kk * 8, dv + TKV::mn_step(kk), id_o, (started || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+        started = true;
+      }
+      if (cur) {
+        const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kStage;
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tS, dq + TQ::k_step(kk), dk + TKV::k_step(kk), id_s, kk > 0 ? 1u : 0u);
+          mma_commit(&bars.s_full[t]);
+        }
+        __syncwarp();
+      }
+      if (elect_one()) {
+        if (i < nsteps) mma_commit(&bars.k_empty[s]);
+        if (prev >= 0) mma_commit(&bars.v_empty[prev % NSV]);
+      }
+      __syncwarp();
+      pend = cur;
     }
+    if (ok && elect_one()) mma_commit(&bars.o_done[t]);
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax (tile t)
-    const int t = warp / 4;
-    const int quad = warp % 4;
+    const int t = (warp - kFirstSoftmaxWarp) / 4;
+    const int quad = warp % 4;  // TMEM lane quadrant this warp may access
     const int r = quad * 32 + lane;
     const int row = pair_row0 + t * kRowsPerTile + r;
     const uint32_t tS = tmem + t * BN;
@@ -329,9 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   static_cast<int64_t>(row < n ? row : 0) * p.mask_row_words
             : nullptr;
     for (int i = 0; i < nsteps && ok; ++i) {
-      const uint32_t cls = (steps[i] >> (16 + 2 * t)) & 3u;
+      const uint32_t sw = step_at(i);
+      const uint32_t cls = (sw >> (16 + 2 * t)) & 3u;
       if (cls == kSkip) continue;
-      const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
+      const int key0 = static_cast<int>(sw & 0xFFFFu) * BN;
       ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
       if (!ok) break;
       s_phase ^= 1;
@@ -496,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemAlloc);
   }

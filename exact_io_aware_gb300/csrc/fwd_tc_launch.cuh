@@ -9,16 +9,13 @@
 namespace ea {
 namespace fwd {
 
-// Opt-in shared memory per CTA on sm_103a is 227 KiB, of which the kernel's static barrier
-// block takes a few hundred bytes.
-constexpr int kMaxDynSmem = 227 * 1024 - 1024;
-
 template <bool kBf16, int D, int BN>
 int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   using Cfg = Config<D, BN>;
-  const size_t smem = Cfg::smem_bytes(a.n);
+  const size_t smem = Cfg::smem_bytes(a.n, a.mask_kind);
   if (smem > static_cast<size_t>(kMaxDynSmem)) {
-    err = "n too large for the forward step table at this key block";
+    err = "n too large for the bitmap step table of the forward at this key block (use a "
+          "smaller kv_block)";
     return -2;
   }
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;

@@ -103,6 +103,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// mbar_wait executed by a whole warp with a warp-uniform result: every lane waits, and the warp
+// proceeds only if every lane saw the phase (so code after it can use warp-collective
+// instructions such as elect.sync).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                               uint32_t site) {
+  const bool ok = mbar_wait(bar, parity, status, site);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // mbar_wait with polling probes (mbar_test_wait); same bound and timeout reporting.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, uint32_t* status,
                                                uint32_t site) {
@@ -131,6 +140,15 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, ui
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Request one box of a 3-D tiled tensor into L2 (no shared memory, no completion to wait on).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 

@@ -49,6 +49,16 @@ struct Tile {
     return smem_desc(base + kk * 16 * L::kRowBytes, kBoxBytes, 8 * L::kRowBytes, L::kSwz);
   }
 
+  // desc_k(base, kk) - desc_k(base, 0) and desc_mn(base, kk) - desc_mn(base, 0): the kk-th
+  // 16-element step only moves the descriptor's start-address field (16-byte units), so a
+  // descriptor built once per buffer serves every step by adding these constants.
+  __host__ __device__ static constexpr uint64_t k_step(int kk) {
+    return static_cast<uint64_t>(((kk * 32) / L::kRowBytes) * kBoxBytes + (kk * 32) % L::kRowBytes) >> 4;
+  }
+  __host__ __device__ static constexpr uint64_t mn_step(int kk) {
+    return static_cast<uint64_t>(kk * 16 * L::kRowBytes) >> 4;
+  }
+
   // Byte offset of element (r, c) inside the swizzled tile (for threads that write operands).
   // The TMA/UMMA swizzle of width RowBytes XORs address bits [4, 4+B) with bits [7, 7+B),
   // B = log2(RowBytes / 16); the tile base is 1024-byte aligned, so offsets suffice.
