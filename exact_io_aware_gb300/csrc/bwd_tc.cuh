@@ -19,11 +19,12 @@
 //   dSᵀ = Pᵀ (dPᵀ - D)                   softmax warps; 16-bit, written over dPᵀ
 //   dV += Pᵀ dO,  dK += dSᵀ Q            (A operand read from tensor memory)
 // Roles:
-//   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. and half w / 4 of the block's query
-//              columns (P and dS are elementwise, so the halves never meet); warps 0-3 also
-//              write dK and dV at the end
-//   warp  8    TMA producer (K, V once; Q, dO, LSE, D per block through an NS-stage ring)
-//   warp  9    TMEM allocator and MMA issuer
+//   warp  0    TMEM allocator and MMA issuer (lowest warp slot: the warp schedulers favour it
+//              over the softmax warps it shares a sub-partition with)
+//   warps 1-8  softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 1) / 4 of the
+//              block's query columns (P and dS are elementwise, so the halves never meet);
+//              warps 1-4 also write dK and dV at the end
+//   warp  9    TMA producer (K, V once; Q, dO, LSE, D per block through an NS-stage ring)
 // Issue order per block i: dV_i, S_{i+1}, dK_i, dP_{i+1}: S_{i+1} follows dV_i, the last reader
 // of P_i, and dP_{i+1} follows dK_i, the last reader of dS_i.
 #pragma once
@@ -40,8 +41,9 @@ constexpr int kKeys = 128;
 constexpr int BQ = 128;  // queries per block
 constexpr int kThreads = 320;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 0;
+constexpr int kFirstSoftmaxWarp = 1;
+constexpr int kProducerWarp = 9;
 constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
 
 struct BwdParams {
@@ -303,66 +305,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);  // Sᵀ, dPᵀ
-      constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);  // dV, dK
-      const uint32_t sk = smem_u32(sK), sv = smem_u32(sV);
-      bool ok = mbar_wait_spin(&bars.kv_full, 0, p.status, 22);
-      auto wait_qdo = [&](int i) -> bool {
-        return mbar_wait_spin(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
-      };
-      auto issue_s = [&](int i) {
-        const uint32_t qb = smem_u32(sQ + (i % NS) * TQ::kBytes);
+    // The whole warp runs the loop so that descriptors stay warp-uniform; one elected lane
+    // issues.  Operand descriptors are built once per buffer: a 16-element step or a ring
+    // stage only adds a constant to the start-address field.
+    constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);  // Sᵀ, dPᵀ
+    constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);  // dV, dK
+    constexpr uint64_t kStage = TQ::kBytes >> 4;
+    const uint64_t dk = TK::desc_k(smem_u32(sK), 0), dv = TK::desc_k(smem_u32(sV), 0);
+    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TQ::desc_k(smem_u32(sG), 0);
+    const uint64_t dqmn0 = TQ::desc_mn(smem_u32(sQ), 0), dgmn0 = TQ::desc_mn(smem_u32(sG), 0);
+    bool ok = mbar_wait_spin_warp(&bars.kv_full, 0, p.status, 22);
+    auto wait_qdo = [&](int i) -> bool {
+      return mbar_wait_spin_warp(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
+    };
+    auto issue_s = [&](int i) {
+      const uint64_t dq = dq0 + static_cast<uint64_t>(i % NS) * kStage;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS, TK::desc_k(sk, kk), TQ::desc_k(qb, kk), id_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::kColS, dk + TK::k_step(kk), dq + TQ::k_step(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars.s_full);
-      };
-      auto issue_dp = [&](int i) {
-        const uint32_t gb = smem_u32(sG + (i % NS) * TQ::kBytes);
+      }
+      __syncwarp();
+    };
+    auto issue_dp = [&](int i) {
+      const uint64_t dg = dg0 + static_cast<uint64_t>(i % NS) * kStage;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, TK::desc_k(sv, kk), TQ::desc_k(gb, kk), id_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::kColDP, dv + TK::k_step(kk), dg + TQ::k_step(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars.dp_full);
-      };
-      if (ok && nsteps > 0) {
-        ok = wait_qdo(0);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-          issue_dp(0);
-        }
       }
-      for (int i = 0; i < nsteps && ok; ++i) {
-        const int s = i % NS;
-        const uint32_t qb = smem_u32(sQ + s * TQ::kBytes);
-        const uint32_t gb = smem_u32(sG + s * TQ::kBytes);
-        ok = mbar_wait_spin(&bars.p_full, i & 1, p.status, 24);
-        if (!ok) break;
+      __syncwarp();
+    };
+    if (ok && nsteps > 0) {
+      ok = wait_qdo(0);
+      if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), TQ::desc_mn(gb, kk), id_kv,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        const bool more = i + 1 < nsteps;
-        if (more) {
-          ok = wait_qdo(i + 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(i + 1);
-        }
-        ok = mbar_wait_spin(&bars.ds_full, i & 1, p.status, 25);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(16 * kk), TQ::desc_mn(qb, kk), id_kv,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.qdo_empty[s]);
-        if (more) issue_dp(i + 1);
+        issue_s(0);
+        issue_dp(0);
       }
-      mma_commit(&bars.kv_done);
     }
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const int s = i % NS;
+      ok = mbar_wait_spin_warp(&bars.p_full, i & 1, p.status, 24);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dgmn = dgmn0 + static_cast<uint64_t>(s) * kStage;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), dgmn + TQ::mn_step(kk),
+                 id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+      const bool more = i + 1 < nsteps;
+      if (more) {
+        ok = wait_qdo(i + 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(i + 1);
+      }
+      ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 25);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dqmn = dqmn0 + static_cast<uint64_t>(s) * kStage;
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(16 * kk), dqmn + TQ::mn_step(kk),
+                 id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.qdo_empty[s]);
+      }
+      __syncwarp();
+      if (more) issue_dp(i + 1);
+    }
+    if (elect_one()) mma_commit(&bars.kv_done);
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax: P and dS
     const int quad = warp % 4;
@@ -370,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j = key0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     constexpr int kHalf = BQ / 2;  // query columns of this warp: [c_lo, c_lo + kHalf)
-    const int c_lo = (warp / 4) * kHalf;
+    const int half = (warp - kFirstSoftmaxWarp) / 4;
+    const int c_lo = half * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
     const uint32_t tS = tmem + C::kColS + lane_off;
     const uint32_t tP = tmem + C::kColDP + lane_off;
@@ -454,9 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ds_full);
     }
-    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // ---------------------------------------------------------------- epilogue (warps 1-4)
     // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
-    if (warp < 4) {
+    if (half == 0) {
       if (ok) ok = mbar_wait_spin(&bars.kv_done, 0, p.status, 31);
       tc_fence_after();
       if (ok) {

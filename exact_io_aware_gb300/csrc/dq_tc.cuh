@@ -18,10 +18,11 @@
 //   dS = P (dP - D)                      softmax warps; 16-bit, written over dP
 //   dQ += dS K_j                         (A operand read from tensor memory)
 // Roles:
-//   warps 0-7  softmax: warp w owns TMEM lanes 32 (w % 4).. and half w / 4 of the block's key
-//              columns; warps 0-3 also write dQ at the end
-//   warp  8    TMA producer (Q, dO once; K and V blocks through an NS-stage ring)
-//   warp  9    TMEM allocator and MMA issuer
+//   warp  0    TMEM allocator and MMA issuer (lowest warp slot: the warp schedulers favour it
+//              over the softmax warps it shares a sub-partition with)
+//   warps 1-8  softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 1) / 4 of the
+//              block's key columns; warps 1-4 also write dQ at the end
+//   warp  9    TMA producer (Q, dO once; K and V blocks through an NS-stage ring)
 // Issue order per block i: [S_{i+1}], dQ_i, [dP_{i+1}]: dP_{i+1} follows dQ_i, the last reader
 // of dS_i.
 #pragma once
@@ -39,8 +40,9 @@ constexpr int kRows = 128;  // query rows per CTA
 constexpr int BN = 128;     // keys per block
 constexpr int kThreads = 320;
 constexpr int kSoftmaxWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 0;
+constexpr int kFirstSoftmaxWarp = 1;
+constexpr int kProducerWarp = 9;
 using bwd::kFull;
 using bwd::kPartial;
 using bwd::kSkip;
@@ -225,51 +227,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);  // S, dP
-      constexpr uint32_t id_q = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dQ
-      const uint32_t qb = smem_u32(sQ), gb = smem_u32(sG);
-      bool ok = nsteps == 0 || mbar_wait_spin(&bars.qg_full, 0, p.status, 43);
-      auto issue_s = [&](int i) -> bool {
-        if (!mbar_wait_spin(&bars.k_full[i % NS], (i / NS) & 1, p.status, 44)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(sK + (i % NS) * TK::kBytes);
+    // The whole warp runs the loop so that descriptors stay warp-uniform; one elected lane
+    // issues.  Operand descriptors are built once per buffer: a 16-element step or a ring
+    // stage only adds a constant to the start-address field.
+    constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);  // S, dP
+    constexpr uint32_t id_q = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dQ
+    constexpr uint64_t kStage = TK::kBytes >> 4;
+    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TQ::desc_k(smem_u32(sG), 0);
+    const uint64_t dk0 = TK::desc_k(smem_u32(sK), 0), dv0 = TK::desc_k(smem_u32(sV), 0);
+    const uint64_t dkmn0 = TK::desc_mn(smem_u32(sK), 0);
+    bool ok = nsteps == 0 || mbar_wait_spin_warp(&bars.qg_full, 0, p.status, 43);
+    auto issue_s = [&](int i) -> bool {
+      if (!mbar_wait_spin_warp(&bars.k_full[i % NS], (i / NS) & 1, p.status, 44)) return false;
+      tc_fence_after();
+      const uint64_t dk = dk0 + static_cast<uint64_t>(i % NS) * kStage;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS + (i & 1) * BN, TQ::desc_k(qb, kk), TK::desc_k(kb, kk), id_s,
+          mma_ss(tmem + C::kColS + (i & 1) * BN, dq0 + TQ::k_step(kk), dk + TK::k_step(kk), id_s,
                  kk > 0 ? 1u : 0u);
         mma_commit(&bars.s_full[i & 1]);
-        return true;
-      };
-      auto issue_dp = [&](int i) -> bool {
-        if (!mbar_wait_spin(&bars.v_full[i % NS], (i / NS) & 1, p.status, 45)) return false;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(sV + (i % NS) * TK::kBytes);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int i) -> bool {
+      if (!mbar_wait_spin_warp(&bars.v_full[i % NS], (i / NS) & 1, p.status, 45)) return false;
+      tc_fence_after();
+      const uint64_t dv = dv0 + static_cast<uint64_t>(i % NS) * kStage;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, TQ::desc_k(gb, kk), TK::desc_k(vb, kk), id_s, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + C::kColDP, dg0 + TQ::k_step(kk), dv + TK::k_step(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars.dp_full);
         mma_commit(&bars.v_empty[i % NS]);
-        return true;
-      };
-      if (ok && nsteps > 0) ok = issue_s(0) && issue_dp(0);
-      for (int i = 0; i < nsteps && ok; ++i) {
-        const bool more = i + 1 < nsteps;
-        if (more) ok = issue_s(i + 1);
-        if (!ok) break;
-        ok = mbar_wait_spin(&bars.ds_full, i & 1, p.status, 46);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(sK + (i % NS) * TK::kBytes);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && nsteps > 0) ok = issue_s(0) && issue_dp(0);
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const bool more = i + 1 < nsteps;
+      if (more) ok = issue_s(i + 1);
+      if (!ok) break;
+      ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 46);
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t dkmn = dkmn0 + static_cast<uint64_t>(i % NS) * kStage;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(16 * kk), TK::desc_mn(kb, kk),
+          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(16 * kk), dkmn + TK::mn_step(kk),
                  id_q, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.k_empty[i % NS]);
-        if (more) ok = issue_dp(i + 1);
       }
-      mma_commit(&bars.dq_done);
+      __syncwarp();
+      if (more) ok = issue_dp(i + 1);
     }
+    if (elect_one()) mma_commit(&bars.dq_done);
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax: P and dS
     const int quad = warp % 4;
@@ -277,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     constexpr int kHalf = BN / 2;  // key columns of this warp: [c_lo, c_lo + kHalf)
-    const int c_lo = (warp / 4) * kHalf;
+    const int half = (warp - kFirstSoftmaxWarp) / 4;
+    const int c_lo = half * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
     // D_i: this warp sums dO * O over its half of the head dimension (16-byte loads)
-    const int half = warp / 4;
     float dpar = 0.0f;
     if (row < n) {
       using E = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
@@ -394,9 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ds_full);
     }
-    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    // ---------------------------------------------------------------- epilogue (warps 1-4)
     // dQ = c * (dS K) rounded and stored through the (now idle) Q tile.
-    if (warp < 4 && row0 < n) {
+    if (half == 0 && row0 < n) {
       if (ok && nsteps > 0) ok = mbar_wait_spin(&bars.dq_done, 0, p.status, 49);
       tc_fence_after();
       if (ok) {

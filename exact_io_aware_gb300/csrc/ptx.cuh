@@ -127,6 +127,13 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, u
   return false;
 }
 
+// mbar_wait_spin executed by a whole warp with a warp-uniform result (see mbar_wait_warp).
+__device__ __forceinline__ bool mbar_wait_spin_warp(uint64_t* bar, uint32_t parity,
+                                                    uint32_t* status, uint32_t site) {
+  const bool ok = mbar_wait_spin(bar, parity, status, site);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // ------------------------------------------------------------------ TMA (tensor maps)
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
