@@ -6,6 +6,7 @@ the current CUDA stream.  All arithmetic runs in the library's CUDA kernels; the
 CPU or PyTorch fallback, and every entry point raises if the library is not built.
 
     o, lse = attn_fwd(q, k, v, c, mask="causal")
+    o, lse = attn_fwd_split(q, k, v, c, mask="causal")   # key shares + merge (few heads)
     dq, dk, dv = attn_bwd(q, k, v, o, lse, do, c, mask="causal")
     y = attention(q, k, v, c, mask="causal")      # autograd-aware wrapper
 """
@@ -21,7 +22,8 @@ __all__ = [
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
     "attn_device_status", "attn_last_error", "attention", "attn_bwd_noalloc",
-    "attn_selftest_wait_timeout",
+    "attn_selftest_wait_timeout", "attn_fwd_split", "attn_fwd_split_count",
+    "attn_fwd_split_workspace_bytes", "attn_merge",
 ]
 
 ATTN_OK = 0
@@ -71,6 +73,15 @@ def load():
     lib.attn_device_status.restype = i32
     lib.attn_last_error.argtypes = []
     lib.attn_last_error.restype = ctypes.c_char_p
+    lib.attn_fwd_split.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
+                                   i32, i32, vp, vp, vp, sz, vp]
+    lib.attn_fwd_split.restype = i32
+    lib.attn_fwd_split_count.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.attn_fwd_split_count.restype = i32
+    lib.attn_fwd_split_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.attn_fwd_split_workspace_bytes.restype = sz
+    lib.attn_merge.argtypes = [i32, i32, i64, i32, vp, vp, vp, vp, vp]
+    lib.attn_merge.restype = i32
     _lib = lib
     return lib
 
@@ -131,6 +142,59 @@ def attn_fwd(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=0, 
     _check(load().attn_fwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
                            kind, _ptr(bits), row_words, hs, int(kv_block), _ptr(o), _ptr(lse),
                            _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_fwd_split_count(dtype, B, H, n, d, kv_block=0) -> int:
+    """Key shares attn_fwd_split uses with num_splits=0 on the current device."""
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().attn_fwd_split_count(code, B, H, n, d, int(kv_block)))
+
+
+def attn_fwd_split_workspace_bytes(dtype, B, H, n, d, num_splits) -> int:
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().attn_fwd_split_workspace_bytes(code, B, H, n, d, int(num_splits)))
+
+
+def attn_fwd_split(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=0,
+                   kv_block=0, num_splits=0, o=None, lse=None, workspace=None, stream=None):
+    """Forward pass over num_splits key shares merged into (o, lse); 0 = library choice."""
+    B, H, n, d = _shape(q, k, v)
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    splits = int(num_splits) or attn_fwd_split_count(q.dtype, B, H, n, d, kv_block)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
+    need = attn_fwd_split_workspace_bytes(q.dtype, B, H, n, d, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(load().attn_fwd_split(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k),
+                                 _ptr(v), kind, _ptr(bits), row_words, hs, int(kv_block), splits,
+                                 _ptr(o), _ptr(lse), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_merge(o_parts, lse_parts, dtype=torch.float32, o=None, lse=None, stream=None):
+    """Merge partial results over disjoint key sets: o_parts [P, ..., d] float32 and
+    lse_parts [P, ...] float32 -> (o [..., d] of ``dtype``, lse [...] float32)."""
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("o_parts and lse_parts must be float32")
+    if not (o_parts.is_cuda and o_parts.is_contiguous() and lse_parts.is_cuda
+            and lse_parts.is_contiguous()):
+        raise ValueError("o_parts and lse_parts must be contiguous CUDA tensors")
+    if o_parts.shape[:-1] != lse_parts.shape:
+        raise ValueError("o_parts must be lse_parts' shape plus a trailing d")
+    parts, d = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    if o is None:
+        o = torch.empty(o_parts.shape[1:], dtype=dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    _check(load().attn_merge(DTYPE_CODE[o.dtype], parts, rows, d, _ptr(o_parts), _ptr(lse_parts),
+                             _ptr(o), _ptr(lse), _stream_ptr(stream)))
     return o, lse
 
 

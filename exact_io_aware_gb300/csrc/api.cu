@@ -2,6 +2,7 @@
 // error reporting and the device status word.  See include/exactattn.h for the contract.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <string>
@@ -48,6 +49,38 @@ int status_ptr(uint32_t** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kMaxSplits = 32;
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Streaming multiprocessors of the current device (looked up once per device).
+int sm_count() {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!cached[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+// Library choice of the key split: enough shares that the forward grid covers every
+// multiprocessor once, at most one share per key block and at most kMaxSplits.
+int auto_splits(int dtype, int B, int H, int n, int kv_block) {
+  const int rows_per_cta = dtype == ATTN_F32 ? 32 : 256;
+  const int bn = kv_block ? kv_block : (dtype == ATTN_F32 ? 64 : 128);
+  const int64_t ctas = static_cast<int64_t>((n + rows_per_cta - 1) / rows_per_cta) * B * H;
+  const int sms = sm_count();
+  int splits = sms > 0 ? static_cast<int>((sms + ctas - 1) / ctas) : 1;
+  splits = std::min(splits, (n + bn - 1) / bn);
+  return std::max(1, std::min(splits, kMaxSplits));
+}
+
+size_t split_part_bytes(int B, int H, int n, int d, int splits) {
+  return round256(static_cast<size_t>(splits) * B * H * n * d * sizeof(float));
+}
+
 int check_common(int dtype, int B, int H, int n, int d, const void* q, const void* k,
                  const void* v, int mask_kind, const uint32_t* bits, int64_t row_words,
                  int64_t head_stride, int kv_block) {
@@ -91,6 +124,7 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.mask_row_words = row_words;
   a.mask_head_stride_words = head_stride;
   a.kv_block = kv_block;
+  a.num_splits = 1;
   return a;
 }
 
@@ -130,6 +164,80 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc = dtype == ATTN_F32 ? ea::launch_fwd_f32(a, s, err)
                              : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
+int attn_fwd_split_count(int dtype, int B, int H, int n, int d, int kv_block) {
+  if (B < 1 || H < 1 || n < 1 || d < 1) return 0;
+  return auto_splits(dtype, B, H, n, kv_block);
+}
+
+size_t attn_fwd_split_workspace_bytes(int dtype, int B, int H, int n, int d, int num_splits) {
+  (void)dtype;
+  if (B < 1 || H < 1 || n < 1 || d < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (num_splits == 1) return 0;
+  return split_part_bytes(B, H, n, d, num_splits) +
+         round256(static_cast<size_t>(num_splits) * B * H * n * sizeof(float));
+}
+
+int attn_fwd_split(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+                   const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                   int64_t mask_head_stride_words, int kv_block, int num_splits, void* o,
+                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(ATTN_ERR_INVALID_ARG, "num_splits must be 0 (library choice) or 1..32");
+  if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
+                            mask_head_stride_words, kv_block))
+    return rc;
+  const int splits = num_splits ? num_splits : auto_splits(dtype, B, H, n, kv_block);
+  if (splits == 1)
+    return attn_fwd(dtype, B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                    mask_head_stride_words, kv_block, o, lse, stream);
+  if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
+  if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  const size_t need = attn_fwd_split_workspace_bytes(dtype, B, H, n, d, splits);
+  if (!workspace || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE,
+                "workspace missing or smaller than attn_fwd_split_workspace_bytes");
+  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  ea::AttnArgs a = make_args(B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                             mask_head_stride_words, kv_block);
+  a.num_splits = splits;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        split_part_bytes(B, H, n, d, splits));
+  if (int rc = status_ptr(&a.status)) return rc;
+  std::string err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = dtype == ATTN_F32 ? ea::launch_fwd_f32(a, s, err)
+                             : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
+  if (rc) return fail(rc, err);
+  rc = ea::launch_merge(dtype, splits, static_cast<int64_t>(B) * H * n, d, a.o_part, a.lse_part,
+                        o, lse, a.status, s, err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
+int attn_merge(int dtype, int num_parts, int64_t rows, int d, const float* o_parts,
+               const float* lse_parts, void* o, float* lse, void* stream) {
+  if (dtype < ATTN_F32 || dtype > ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype");
+  if (num_parts < 1 || rows < 1 || d < 4)
+    return fail(ATTN_ERR_INVALID_ARG, "num_parts and rows must be positive and d >= 4");
+  if (d % 4 != 0) return fail(ATTN_ERR_UNSUPPORTED, "d must be a multiple of 4");
+  if (!o_parts || !lse_parts || !o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(o_parts) || !aligned16(o))
+    return fail(ATTN_ERR_ALIGNMENT, "o_parts and o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse_parts) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse_parts and lse must be 4-byte aligned");
+  uint32_t* st = nullptr;
+  if (int rc = status_ptr(&st)) return rc;
+  std::string err;
+  int rc = ea::launch_merge(dtype, num_parts, rows, d, o_parts, lse_parts, o, lse, st,
+                            static_cast<cudaStream_t>(stream), err);
   if (rc) return fail(rc, err);
   return ATTN_OK;
 }

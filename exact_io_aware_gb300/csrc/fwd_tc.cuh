@@ -22,6 +22,11 @@
 // The issuers have the lowest warp slots, which the warp schedulers favour over the
 // softmax warps they share a sub-partition with.
 //
+// Key split (gridDim.z > 1): the pair's key blocks are cut into gridDim.z contiguous shares and
+// CTA z walks share z only.  It writes its rows' summary of that share in normalised form,
+// O_z = z/l (float32) and LSE_z = m + ln l (-inf for a row with no allowed key in the share),
+// which a merge kernel combines by the merge rule of the stable summaries.
+//
 // Online softmax (the running-maximum recurrence of "The Arithmetic of Intelligence",
 // chapter 12): scores are taken to base 2 with the folded factor c·log2(e) (the exp2
 // prescale described in "Bellek Duvarının Fiziği", online softmax section).  The running
@@ -152,6 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair = (gridDim.x - 1 - blockIdx.x);  // heaviest (causal) query tiles first
   const int pair_row0 = pair * 2 * kRowsPerTile;  // tile t starts at pair_row0 + 128 t
   const int nblk = (n + BN - 1) / BN;
+  const int split = blockIdx.z;
+  const int nsplit = gridDim.z;
+  const bool partial_out = p.o_part != nullptr;
 
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
@@ -166,11 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
 
-  // Walk over key blocks.  Under a bitmap mask every block is classified for both tiles (skip /
-  // full / partial) into a table of the blocks some tile takes; otherwise step i is block i,
-  // up to the last block the pair's rows reach.
+  // Walk over key blocks.  Under a bitmap mask every block of this CTA's share is classified
+  // for both tiles (skip / full / partial) into a table of the blocks some tile takes;
+  // otherwise step i is block j_lo + i, up to the last block of the share.
   const bool use_table = p.mask_kind == kMaskBitmap;
   const bool causal = p.mask_kind == kMaskCausal;
+  const int pair_last = min(pair_row0 + 2 * kRowsPerTile, n) - 1;  // last row of the pair
+  const int reach = use_table ? nblk : (causal ? pair_last / BN + 1 : nblk);  // blocks walked
+  const int share = (reach + nsplit - 1) / nsplit;
+  const int j_lo = min(split * share, reach);
+  const int j_hi = min(j_lo + share, reach);
   if (use_table) {
     for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
     __syncthreads();
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t* rowbits =
           p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
           static_cast<int64_t>(valid ? row : 0) * p.mask_row_words;
-      for (int j = 0; j < nblk; ++j) {
+      for (int j = j_lo; j < j_hi; ++j) {
         bool any = false, all = true;
         if (valid) {
 #pragma unroll
@@ -209,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
       const bool tail = (n % BN) != 0;
       int ns = 0;
-      for (int j = 0; j < nblk; ++j) {
+      for (int j = j_lo; j < j_hi; ++j) {
         const uint32_t b = steps[j];
         const bool part_tail = tail && j == nblk - 1;
         uint32_t cls0 = (b & 1u) ? (((b & 4u) || part_tail) ? kPartial : kFull) : kSkip;
@@ -223,10 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bars.act = act;
     }
   } else if (tid == 0) {
-    const int last = min(pair_row0 + 2 * kRowsPerTile, n) - 1;  // last row of the pair
-    bars.nsteps = causal ? last / BN + 1 : nblk;
-    // every tile with rows takes block 0
-    bars.act = (pair_row0 < n ? 1u : 0u) | (pair_row0 + kRowsPerTile < n ? 2u : 0u);
+    bars.nsteps = j_hi - j_lo;
+    // a tile with rows takes every block of the share up to the last one its rows reach
+    uint32_t act = 0;
+    for (int t = 0; t < 2; ++t) {
+      const int r0 = pair_row0 + t * kRowsPerTile;
+      if (r0 >= n || j_lo >= j_hi) continue;
+      const int last_blk = causal ? (min(r0 + kRowsPerTile, n) - 1) / BN : nblk - 1;
+      if (j_lo <= last_blk) act |= 1u << t;
+    }
+    bars.act = act;
   }
   if (tid == 0) {
     // A ring stage is free once the MMA warp of every active tile has released it.
@@ -244,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t act = bars.act;
   // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*D
   auto step_at = [&](int i) -> uint32_t {
-    return use_table ? steps[i] : dense_step(i, BN, nblk, n, pair_row0, causal);
+    return use_table ? steps[i] : dense_step(j_lo + i, BN, nblk, n, pair_row0, causal);
   };
 
   if (warp == kProducerWarp) {
@@ -392,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.0f;       // running normaliser relative to m
     uint32_t s_phase = 0;
     bool first = true;
-    bool ok = active;
+    bool ok = true;  // false once a bounded wait gave up; an inactive tile skips every step
     const uint32_t* rowbits =
         p.mask_kind == kMaskBitmap
             ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
@@ -519,9 +538,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars.p_full[t]);
     }
     // ---------------------------------------------------------------- epilogue
-    // A tile with rows but no allowed key at all (possible only under a bitmap) writes zeros
-    // and -inf, like any other row with an empty allowed set.
-    if (pair_row0 + t * kRowsPerTile < n) {
+    if (partial_out) {
+      // Key split: this share's normalised partial, float32, one row per thread.  A row with
+      // no allowed key in the share gets O_z = 0 and LSE_z = -inf (not an empty row overall).
+      if (pair_row0 + t * kRowsPerTile < n) {
+        if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
+        tc_fence_after();
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        // The TMEM loads are warp-collective: every lane takes part, rows past n included;
+        // only the stores are per row.
+        if (ok) {
+          const int64_t prow = (static_cast<int64_t>(split) * gridDim.y + bh) * n + row;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t rr[16];
+            if (active) {
+              tmem_ld16(tO + lane_off + c0, rr);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int k = 0; k < 16; ++k) rr[k] = 0u;
+            }
+            if (row < n) {
+#pragma unroll
+              for (int k = 0; k < 16; k += 4)
+                dst[(c0 + k) / 4] =
+                    make_float4(__uint_as_float(rr[k]) * inv, __uint_as_float(rr[k + 1]) * inv,
+                                __uint_as_float(rr[k + 2]) * inv, __uint_as_float(rr[k + 3]) * inv);
+            }
+          }
+          if (row < n)
+            p.lse_part[prow] = l > 0.0f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
+        }
+      }
+    } else if (pair_row0 + t * kRowsPerTile < n) {
+      // A tile with rows but no allowed key at all (possible only under a bitmap) writes zeros
+      // and -inf, like any other row with an empty allowed set.
       if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
       tc_fence_after();
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;

@@ -35,9 +35,12 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
     err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
     return -5;
   }
+  const int nsplit = a.num_splits > 1 ? a.num_splits : 1;
   FwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
-              a.lse, a.status};
-  dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads));
+              a.lse, a.status, nsplit, nsplit > 1 ? a.o_part : nullptr,
+              nsplit > 1 ? a.lse_part : nullptr};
+  dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads),
+            static_cast<unsigned>(nsplit));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) {

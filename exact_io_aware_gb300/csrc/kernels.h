@@ -20,6 +20,12 @@ struct FwdParams {
   int64_t mask_head_stride_words;
   float* lse;
   uint32_t* status;
+  // Key-split forward (gridDim.z = num_splits > 1): CTA z walks only its share of the key
+  // blocks and writes the normalised partial O_z (float32, [num_splits][B*H][n][d]) and its
+  // LSE_z ([num_splits][B*H][n], -inf where no allowed key fell in the share) instead of o, lse.
+  int num_splits;
+  float* o_part;
+  float* lse_part;
 };
 
 // Everything a launcher needs; pointers are device pointers.
@@ -44,6 +50,9 @@ struct AttnArgs {
   void* workspace;
   size_t workspace_bytes;
   uint32_t* status;
+  int num_splits;   // forward: 1, or the number of key shards (partials go to o_part, lse_part)
+  float* o_part;
+  float* lse_part;
 };
 
 // Each launcher returns 0 or a negative ATTN_ERR_* code and fills `err` on failure.
@@ -51,6 +60,12 @@ int launch_fwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err
 int launch_bwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err);
 int launch_fwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
 int launch_bwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
+
+// O = sum_g exp(LSE_g - LSE) O_g, LSE = ln sum_g exp(LSE_g) over num_parts partial results
+// (float32 o_part [parts][rows][d], lse_part [parts][rows]); o in the output dtype.
+int launch_merge(int dtype_out, int num_parts, int64_t rows, int d, const float* o_part,
+                 const float* lse_part, void* o, float* lse, uint32_t* status, cudaStream_t s,
+                 std::string& err);
 
 // D_i = sum_a dO[i][a] * O[i][a] for float32 inputs.
 int launch_bwd_pre_f32(const AttnArgs& a, float* D, cudaStream_t s, std::string& err);

@@ -4,8 +4,8 @@
 // framework that owns every device allocation and gives its plugins no allocator, or a
 // system that fixes its whole memory budget at start-up and forbids cudaMalloc afterwards.
 // Such callers can pass inputs and outputs they already own, but not the float32 scratch
-// (D and the dQ accumulator) that attn_bwd expects in `workspace`.  This entry point takes
-// that scratch from one file-scope device array instead.
+// (the per-row table of LSE*log2(e) and D) that attn_bwd expects in `workspace`.  This entry
+// point takes that scratch from one file-scope device array instead.
 //
 // Facts a caller must know:
 //  * The array is kScratchBytes (32 MiB) of device memory.  Every GPU on which this library is
@@ -16,7 +16,7 @@
 //    cudaGetSymbolAddress while that device is current; make that first call before any
 //    stream capture on the device.
 //  * All calls share the one array and it keeps the last call's contents.  Each call rewrites
-//    D and clears the dQ accumulator before use, so stale contents never leak into results,
+//    the whole table before reading it, so stale contents never leak into results,
 //    but two calls whose work overlaps on the GPU (different streams, no ordering between
 //    them) race on the array and give wrong gradients.  Order such calls on one stream.
 //  * It calls no cudaMalloc, cudaFree or allocating library routine; everything else behaves

@@ -10,6 +10,9 @@
 // summary.  A block with no allowed key leaves the summary unchanged.  Lanes take keys for the
 // scores and output columns for the value sums.
 //
+// Key split (gridDim.z > 1): CTA z walks only its share of the key blocks and writes its rows'
+// normalised partial (O_z, LSE_z) to the split buffers; a merge kernel combines the shares.
+//
 // Backward: two kernels, no atomics.  The dQ kernel walks key blocks past 32 query rows; the
 // dK/dV kernel walks query blocks past 32 key rows.  Both recompute s_ij and
 // p_ij = exp(s_ij - LSE_i) and use D_i = dO_i . O_i from the preprocessing kernel.
@@ -72,6 +75,8 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
   const int row_base = blockIdx.x * kRows;
   const size_t head = static_cast<size_t>(bh) * n * D;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool partial_out = gridDim.z > 1;  // O, lse point at the split buffers
+  const size_t out_head = (static_cast<size_t>(blockIdx.z) * gridDim.y + bh) * n;
 
   for (int e = threadIdx.x; e < kRows * D; e += blockDim.x) {
     const int r = e / D, col = e % D;
@@ -87,7 +92,11 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
   }
   const int last_row = min(row_base + kRows, n) - 1;
   const int key_end = mk.kind == kMaskCausal ? last_row + 1 : n;
-  for (int key0 = 0; key0 < key_end; key0 += BN) {
+  const int reach = (key_end + BN - 1) / BN;  // key blocks the rows reach
+  const int share = (reach + gridDim.z - 1) / gridDim.z;
+  const int kb_lo = min(static_cast<int>(blockIdx.z) * share, reach);
+  const int kb_hi = min(kb_lo + share, reach);
+  for (int key0 = kb_lo * BN; key0 < kb_hi * BN; key0 += BN) {
     __syncthreads();
     for (int e = threadIdx.x; e < BN * D; e += blockDim.x) {
       const int j = e / D, col = e % D;
@@ -149,11 +158,11 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
 #pragma unroll
     for (int w = 0; w < NU; ++w) {
       const int col = w * 32 + lane;
-      if (col < D) O[head + static_cast<size_t>(i) * D + col] = z[q][w] * inv;
+      if (col < D) O[(out_head + i) * D + col] = z[q][w] * inv;
     }
     if (lane == 0) {
-      lse[static_cast<size_t>(bh) * n + i] = empty ? -INFINITY : m[q] + logf(l[q]);
-      if (empty) raise_empty_row(status);
+      lse[out_head + i] = empty ? -INFINITY : m[q] + logf(l[q]);
+      if (empty && !partial_out) raise_empty_row(status);
     }
   }
 }
@@ -367,10 +376,12 @@ int fwd_run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   const size_t smem = sizeof(float) * (kRows * D + BN * (D + 1) + BN * D);
   auto k = fwd_kernel<D, BN>;
   if (int rc = set_smem(k, smem, err)) return rc;
-  dim3 grid((a.n + kRows - 1) / kRows, a.B * a.H);
+  const bool split = a.num_splits > 1;
+  dim3 grid((a.n + kRows - 1) / kRows, a.B * a.H, split ? a.num_splits : 1);
   k<<<grid, kWarps * 32, smem, s>>>(static_cast<const float*>(a.q), static_cast<const float*>(a.k),
-                                    static_cast<const float*>(a.v), static_cast<float*>(a.o_out),
-                                    a.lse, a.c, make_mask(a), a.status);
+                                    static_cast<const float*>(a.v),
+                                    split ? a.o_part : static_cast<float*>(a.o_out),
+                                    split ? a.lse_part : a.lse, a.c, make_mask(a), a.status);
   return 0;
 }
 

@@ -40,6 +40,8 @@ def main(argv=None):
     ap.add_argument("--kv-block", type=int, default=0)
     ap.add_argument("--iters", type=int, default=2)
     ap.add_argument("--fwd-only", action="store_true")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="forward through attn_fwd_split with this many key shares (0 = library choice)")
     ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
 
@@ -72,10 +74,19 @@ def main(argv=None):
     o = torch.empty_like(q)
     lse = torch.empty(shape[:3], device="cuda", dtype=torch.float32)
     ws = torch.empty(ea.attn_bwd_workspace_bytes(dt, *shape), dtype=torch.uint8, device="cuda")
+    splits, fws = 1, None
+    if a.splits is not None:
+        splits = a.splits or ea.attn_fwd_split_count(dt, *shape, kv_block=kvb)
+        fws = torch.empty(max(16, ea.attn_fwd_split_workspace_bytes(dt, *shape, splits)),
+                          dtype=torch.uint8, device="cuda")
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.iters + 1)]
     for e in ev:
         e[0].record()
-        ea.attn_fwd(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse)
+        if a.splits is None:
+            ea.attn_fwd(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse)
+        else:
+            ea.attn_fwd_split(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse,
+                              num_splits=splits, workspace=fws)
         e[1].record()
         if not fwd_only:
             ea.attn_bwd(q, k, v, o, lse, do, c, mask=mask, mask_bits=bits, kv_block=kvb,
@@ -87,7 +98,7 @@ def main(argv=None):
     bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev[1:]])) if not fwd_only else None
     fl = 4.0 * B * H * n * n * d * kappa
     out = {"workload": name, "B": B, "H": H, "n": n, "d": d, "dtype": dtype, "mask": mask,
-           "kv_block": kvb, "kappa": kappa, "fwd_ms": fwd_ms,
+           "kv_block": kvb, "splits": splits, "kappa": kappa, "fwd_ms": fwd_ms,
            "fwd_tflops": fl / (fwd_ms / 1e3) / 1e12, "status": status}
     if bwd_ms is not None:
         out.update(bwd_ms=bwd_ms, bwd_tflops=2.5 * fl / (bwd_ms / 1e3) / 1e12)

@@ -95,6 +95,56 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c,
              int64_t mask_head_stride_words, int kv_block,
              void* o, float* lse, void* stream);
 
+/*
+ * Key-split forward: the same O and LSE as attn_fwd, computed as num_splits partial results
+ * over disjoint shares of the key blocks and combined by attn_merge's rule.  This is the
+ * key-sharded reading of the merge of stable summaries in "Exact tiled attention and
+ * memory-aware differentiation": the summary of a union of disjoint key sets is the merge of
+ * the sets' summaries, so the shares can run in parallel.  It fills the GPU when B * H * n is
+ * small next to the key length (few heads, long rows), where attn_fwd launches too few CTAs.
+ *   num_splits  0 = library choice (attn_fwd_split_count), else 1..32; 1 runs attn_fwd
+ *   workspace   device buffer of at least attn_fwd_split_workspace_bytes(...) bytes for the
+ *               number of splits actually used, 16-byte aligned (ignored when that is 1); it
+ *               holds the float32 partial O and LSE of every share and is overwritten
+ *   Other arguments, outputs and errors as for attn_fwd.  Two launches on `stream`.
+ * Each row's key blocks are cut into num_splits contiguous shares of equal block count (the
+ * blocks its rows reach under the causal mask); a row with no allowed key in a share takes
+ * that share as the empty summary.  Results agree with attn_fwd up to rounding.
+ */
+int attn_fwd_split(int dtype, int B, int H, int n, int d, float c,
+                   const void* q, const void* k, const void* v,
+                   int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                   int64_t mask_head_stride_words, int kv_block, int num_splits,
+                   void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The number of key shares attn_fwd_split uses when num_splits = 0 on the current device:
+ * enough that the forward grid covers every multiprocessor, at most one per key block and
+ * at most 32.  0 for non-positive sizes. */
+int attn_fwd_split_count(int dtype, int B, int H, int n, int d, int kv_block);
+
+/* Bytes of workspace attn_fwd_split needs with num_splits shares (1..32; 0 bytes for 1):
+ * float32 partial outputs [num_splits][B][H][n][d] and LSEs [num_splits][B][H][n], each
+ * rounded up to 256 bytes. */
+size_t attn_fwd_split_workspace_bytes(int dtype, int B, int H, int n, int d, int num_splits);
+
+/*
+ * Merge partial attention results over disjoint key sets into the result over their union
+ * (the merge rule of the stable summaries, "Exact tiled attention and memory-aware
+ * differentiation"; key-sharded attention combines shards this way).  For each of `rows`
+ * rows, with parts g = 0 .. num_parts-1 given in normalised form (O_g, LSE_g):
+ *     LSE = M + ln sum_g exp(LSE_g - M),  M = max_g LSE_g
+ *     O   = sum_g exp(LSE_g - LSE) O_g
+ * A part with LSE_g = -inf is an empty key set and contributes nothing; a row whose parts are
+ * all empty is written as O = 0, LSE = -inf and raises ATTN_WARN_EMPTY_ROW.
+ *   dtype      type of o (ATTN_F32 / ATTN_F16 / ATTN_BF16)
+ *   o_parts    device float32 [num_parts][rows][d], 16-byte aligned; d a multiple of 4
+ *   lse_parts  device float32 [num_parts][rows] (natural log)
+ *   o, lse     device outputs [rows][d] (dtype) and [rows] (float32)
+ * Memory-bound, one launch on `stream`; inputs are only read.
+ */
+int attn_merge(int dtype, int num_parts, int64_t rows, int d, const float* o_parts,
+               const float* lse_parts, void* o, float* lse, void* stream);
+
 /* Bytes of device workspace attn_bwd needs for these sizes: 16-bit types, a per-row table of
  * float32 LSE*log2(e) and D with n rounded up to 128 rows per head; float32, per-row D. */
 size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int n, int d);
@@ -123,13 +173,14 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c,
  * and allows no cudaMalloc afterwards.  The pages have no counterpart to this entry point; it
  * computes exactly what attn_bwd computes.
  *
- * The float32 scratch (D and the dQ accumulator) lives in one static device array of
+ * The float32 scratch (the per-row table of LSE*log2(e) and D that attn_bwd keeps in its
+ * workspace) lives in one static device array of
  * ATTN_BWD_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU which loads this library holds
  * until the process exits.  A problem with attn_bwd_workspace_bytes(...) larger than that
  * is rejected with ATTN_ERR_WORKSPACE (see attn_last_error) before anything runs.  The first
  * call on a device looks up the array's address on that device (cudaGetSymbolAddress); make
  * it before any stream capture there.  All calls share the array, which keeps the last
- * call's contents; each call rewrites and clears what it reads, but calls that overlap on the
+ * call's contents; each call rewrites the table before reading it, but calls that overlap on the
  * GPU (unordered streams) race on it.  No cudaMalloc, cudaFree or allocating library call is
  * made.  Other arguments, outputs and errors as for attn_bwd.
  */

@@ -18,6 +18,11 @@ vector-Jacobian products"):
   s_ij, p_ij = e^{s_ij - m_i}/ℓ_i, γ_ij = p_ij (G_i·V_j - δ_i), then add c γ_ij K_j to dQ_i,
   c γ_ij Q_i to dK_j and p_ij G_i to dV_j.
 
+Key-sharded forward (same page, the merge read as combining shards): the summaries of
+disjoint key sets merge into the summary of their union, so a row's keys can be cut into
+shares, each share summarised on its own, and the shares merged.  ``merge_normalised`` takes
+the shares in the normalised form a kernel writes (O_g = z_g / ℓ_g, LSE_g = m_g + ln ℓ_g).
+
 Indices here are 0-based.  The streaming-softmax recurrence of "The Arithmetic of
 Intelligence", chapter 12 (running max m, running sum ℓ, rescale by e^{m-m'}) is the same
 merge with a block's own summary, so ``streaming_normaliser`` reuses ``merge``.
@@ -119,3 +124,38 @@ def reverse_head(q, k, v, c, allowed, b, Y, m, ell, G):
                 dK[j] += c * gamma * q[i]
                 dV[j] += p * G[i]
     return dQ, dK, dV
+
+
+def merge_normalised(parts):
+    """(O, LSE) of the union of disjoint key sets from the sets' normalised results.
+
+    ``parts`` holds (O_g, LSE_g) for one query row: O_g = z_g / ℓ_g and LSE_g = m_g + ln ℓ_g
+    of key set S_g, or LSE_g = -inf for a set with no allowed key (then O_g is ignored).  The
+    summaries (m, ℓ, z) and (m + ln ℓ, 1, z / ℓ) give the same z / ℓ and the same m + ln ℓ, the
+    two things the forward keeps, so a part enters ``merge`` as (LSE_g, 1, O_g) and an empty
+    part as ⊥.  Returns O = z / ℓ and LSE = m + ln ℓ of the merged summary, or (zeros, -inf)
+    when every part is empty.
+    """
+    state = BOTTOM
+    width = None
+    for o_g, lse_g in parts:
+        o_g = np.asarray(o_g, dtype=np.float64).reshape(-1)
+        width = o_g.size
+        if lse_g == -math.inf:
+            continue
+        state = merge(state, (float(lse_g), 1.0, o_g))
+    if state is BOTTOM:
+        return np.zeros(width or 0), -math.inf
+    m, ell, z = state
+    return z / ell, m + math.log(ell)
+
+
+def key_shares(reach, parts, b):
+    """Key-index ranges of ``parts`` contiguous shares of the first ``reach`` key blocks of
+    size b (equal block counts, the last shares possibly short or empty)."""
+    share = -(-reach // parts)
+    out = []
+    for g in range(parts):
+        lo, hi = min(g * share, reach), min((g + 1) * share, reach)
+        out.append(np.arange(lo * b, hi * b))
+    return out

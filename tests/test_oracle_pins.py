@@ -105,6 +105,59 @@ def test_merge_of_disjoint_sets_is_summary_of_union():
         assert u[0] == s.max()
 
 
+# ---------------------------------------------------------------- key shares (page 5)
+
+def _shard_results(q, k, val, c, a, shares):
+    """Each share's normalised (O_g, LSE_g) from the dense definition on that share alone."""
+    out = []
+    for idx in shares:
+        keep = np.zeros(a.shape[1], bool)
+        keep[idx[idx < a.shape[1]]] = True
+        y, lse, _, _ = attention.forward_rows(q, k, val, c, a & keep[None, :])
+        out.append((y, lse))
+    return out
+
+
+@pytest.mark.parametrize("kind", ["none", "causal", "random"])
+def test_merged_key_shares_equal_dense(kind):
+    rng = _rng(31)
+    n, d, v, b = 45, 4, 3, 4
+    q, k = rng.normal(size=(n, d)), rng.normal(size=(n, d)) * 2
+    val = rng.normal(size=(n, v))
+    c = 0.9
+    if kind == "none":
+        a = np.ones((n, n), bool)
+    elif kind == "causal":
+        a = masks.causal(n)(0, np.arange(n))
+    else:
+        a = _random_allowed(rng, n, 0.15)  # many (row, share) pairs with no allowed key
+    y, lse, _, _ = attention.forward_rows(q, k, val, c, a)
+    reach = -(-n // b)
+    for parts in (1, 2, 3, 5, 12, 20):
+        shares = tiled.key_shares(reach, parts, b)
+        assert sorted(np.concatenate(shares).tolist()) == list(range(reach * b))
+        res = _shard_results(q, k, val, c, a, shares)
+        for i in range(n):
+            o_i, l_i = tiled.merge_normalised([(yg[i], lg[i]) for yg, lg in res])
+            assert abs(l_i - lse[i]) <= 1e-12
+            assert np.max(np.abs(o_i - y[i])) <= 1e-12
+
+
+def test_merge_normalised_worked_example_and_empty_parts():
+    # page 1's blocks {2, 1} and {3, 0} as two shares of one row (zero-width values)
+    l1, l2 = math.log(math.exp(2) + math.exp(1)), math.log(math.exp(3) + 1.0)
+    o, lse = tiled.merge_normalised([(np.zeros(0), l1), (np.zeros(0), l2)])
+    assert abs(lse - (3 + math.log(1.5530017928))) < 1e-9  # m = 3, l = 1.553 as printed
+    assert abs(lse - 3.4401896986) < 1e-9
+    # values: the merged output is the softmax-weighted mean of the shares' outputs
+    o, lse = tiled.merge_normalised([(np.array([1.0, -2.0]), 0.0), (np.array([3.0, 4.0]), math.log(3)),
+                                     (np.array([9.0, 9.0]), -math.inf)])
+    assert abs(lse - math.log(4)) < 1e-15
+    assert np.allclose(o, [(1 + 3 * 3) / 4, (-2 + 3 * 4) / 4], atol=1e-15)
+    o, lse = tiled.merge_normalised([(np.ones(3), -math.inf), (np.ones(3), -math.inf)])
+    assert lse == -math.inf and np.all(o == 0)
+
+
 # ---------------------------------------------------------------- exactness (page 5)
 
 @pytest.mark.parametrize("kind", ["none", "causal", "random"])
