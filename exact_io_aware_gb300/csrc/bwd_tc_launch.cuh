@@ -16,9 +16,9 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   using QCfg = dq::Config<D>;
   const bool bitmap = a.mask_kind == kMaskBitmap;
   const size_t smem = Cfg::smem_bytes(a.n, bitmap);
-  const size_t qsmem = QCfg::smem_bytes(a.n);
+  const size_t qsmem = QCfg::smem_bytes(a.n, bitmap);
   if (smem > static_cast<size_t>(kMaxDynSmem) || qsmem > static_cast<size_t>(kMaxDynSmem)) {
-    err = "n too large for the backward step tables";
+    err = "n too large for the backward step tables under a bitmap mask at this head dimension";
     return -2;
   }
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;

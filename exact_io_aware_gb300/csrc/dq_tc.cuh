@@ -12,19 +12,25 @@
 // the columns) and writes the row table (LSE_i log2 e and D_i) that the dK/dV kernel, launched
 // after it, copies per query block.
 // Per key block j:
-//   S  = Q K_jᵀ           (tensor memory, one query row per lane; two buffers)
+//   S  = Q K_jᵀ           (tensor memory, one query row per lane; one buffer, free again as
+//                          soon as the softmax warps have loaded it)
 //   P  = exp2(S c log2e - LSE log2e)     softmax warps, kept in registers
-//   dP = dO V_jᵀ
+//   dP = dO V_jᵀ          (two buffers, so dP_{j+1} is computed while dQ_j reads dS_j)
 //   dS = P (dP - D)                      softmax warps; 16-bit, written over dP
 //   dQ += dS K_j                         (A operand read from tensor memory)
-// Roles:
-//   warp  0    TMEM allocator and MMA issuer (lowest warp slot: the warp schedulers favour it
-//              over the softmax warps it shares a sub-partition with)
-//   warps 1-8  softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 1) / 4 of the
-//              block's key columns; warps 1-4 also write dQ at the end
-//   warp  9    TMA producer (Q, dO once; K and V blocks through an NS-stage ring)
-// Issue order per block i: [S_{i+1}], dQ_i, [dP_{i+1}]: dP_{i+1} follows dQ_i, the last reader
-// of dS_i.
+// Roles (the control warps take the lowest warp slots, which the warp schedulers favour over
+// the softmax warps they share a sub-partition with):
+//   warp  0    TMEM allocator and MMA issuer
+//   warp  1    TMA producer of Q, dO (once) and the K ring (NSK stages); blocks a few steps
+//              ahead are requested into L2
+//   warp  2    TMA producer of the V ring (NSV stages): the two rings are released by
+//              different products (K after dQ, V after dP), so neither waits on the other
+//   warps 3-10 softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 3) / 4 of the
+//              block's key columns; warps 3-6 also write dQ at the end
+// Issue order per block i: [S_{i+1} once S_i is loaded], [dP_{i+1}], dQ_i.  dP_{i+1} goes to the
+// buffer that dQ_{i-1}, issued before it, read; so the softmax warps find dP_{i+1} ready when
+// they finish dS_i, and the tensor core runs dQ_i while they work on block i+1.  K is held
+// from S_i to dQ_i, across two issue rounds, hence its deeper ring.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,11 +44,13 @@ namespace dq {
 
 constexpr int kRows = 128;  // query rows per CTA
 constexpr int BN = 128;     // keys per block
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 0;
-constexpr int kFirstSoftmaxWarp = 1;
-constexpr int kProducerWarp = 9;
+constexpr int kKProducerWarp = 1;
+constexpr int kVProducerWarp = 2;
+constexpr int kFirstSoftmaxWarp = 3;
+constexpr int kPrefetch = 4;  // key blocks requested into L2 ahead of the ring loads
 using bwd::kFull;
 using bwd::kPartial;
 using bwd::kSkip;
@@ -54,34 +62,35 @@ template <int D>
 struct Config {
   using TQ = Tile<kRows, D>;  // Q, dO (and dQ staging)
   using TK = Tile<BN, D>;     // K, V stages
-  // tensor-memory columns: S buffers, dP, dQ
-  static constexpr int kColS = 0;  // buffer b at b * BN
-  static constexpr int kColDP = 2 * BN;
+  // tensor-memory columns: S, dP buffers, dQ
+  static constexpr int kColS = 0;
+  static constexpr int kColDP = BN;  // buffer b at BN + b * BN
   static constexpr int kColDQ = 3 * BN;
   static constexpr int kTmemCols = kColDQ + pad32(D);
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   static constexpr int kTmemAlloc = 512;
-  static constexpr int kBudget = 227 * 1024 - 2048;
-  static constexpr int kMaxStepBytes = 4 * 1024;
+  static constexpr int kBudget = 227 * 1024 - 2048;  // dynamic limit less alignment slack
   static constexpr int kFixed = 2 * TQ::kBytes;
-  static constexpr int kStage = 2 * TK::kBytes;
-  static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes) / kStage;
-  static constexpr int NS = kFit > 4 ? 4 : kFit;
-  static_assert(NS >= 2, "need two key stages");
+  static constexpr int kStepReserve = 1024;  // smallest step table kept room for (bitmap masks)
+  static constexpr int kSlots = (kBudget - kFixed - kStepReserve) / TK::kBytes;
+  static constexpr int NSV = kSlots / 2 > 4 ? 4 : kSlots / 2;
+  static constexpr int NSK = kSlots - NSV > 4 ? 4 : kSlots - NSV;
+  static_assert(NSV >= 2 && NSK >= 2, "need two key and two value stages");
   static constexpr int kOffQ = 0;
   static constexpr int kOffG = kOffQ + TQ::kBytes;
   static constexpr int kOffK = kOffG + TQ::kBytes;
-  static constexpr int kOffV = kOffK + NS * TK::kBytes;
-  static constexpr int kOffSteps = kOffV + NS * TK::kBytes;
-  static size_t smem_bytes(int n) {
-    return 1024 + kOffSteps + 4 * static_cast<size_t>((n + BN - 1) / BN);
+  static constexpr int kOffV = kOffK + NSK * TK::kBytes;
+  static constexpr int kOffSteps = kOffV + NSV * TK::kBytes;
+  // Only a bitmap mask needs the step table; the walk under the other masks is computed.
+  static size_t smem_bytes(int n, bool bitmap) {
+    return 1024 + kOffSteps + (bitmap ? 4 * static_cast<size_t>((n + BN - 1) / BN) : 0);
   }
 };
 
 struct Barriers {
   uint64_t qg_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[2], dp_full, ds_full;
+  uint64_t s_full, s_free, dp_full[2], ds_full;
   uint64_t dq_done;
   uint32_t tmem_base;
   uint32_t nsteps;
@@ -96,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Config<D>;
   using TQ = typename C::TQ;
   using TK = typename C::TK;
-  constexpr int NS = C::NS;
+  constexpr int NSK = C::NSK;
+  constexpr int NSV = C::NSV;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = bwd::align1024(smem_raw);
@@ -119,26 +129,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
     mbar_init(&bars.qg_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(&bars.v_full[s], 1);
       mbar_init(&bars.v_empty[s], 1);
     }
-    mbar_init(&bars.s_full[0], 1);
-    mbar_init(&bars.s_full[1], 1);
-    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, kSoftmaxWarps);
+    mbar_init(&bars.dp_full[0], 1);
+    mbar_init(&bars.dp_full[1], 1);
     mbar_init(&bars.ds_full, kSoftmaxWarps);
     mbar_init(&bars.dq_done, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
 
-  // Classify each key block for this query tile: skip / full / partial (mask needed).
-  for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
-  __syncthreads();
+  // Walk over key blocks.  Under a bitmap mask every block is classified (skip / full /
+  // partial) into a table of the blocks the tile takes; otherwise step i is block i, up to the
+  // last block the tile's rows reach, and is classified on the fly.
+  const bool use_table = p.mask_kind == kMaskBitmap;
+  const bool causal = p.mask_kind == kMaskCausal;
   const int last_row = min(row0 + kRows, n) - 1;
-  if (p.mask_kind == kMaskBitmap) {
+  if (use_table) {
+    for (int j = tid; j < nblk; j += kThreads) steps[j] = 0;
+    __syncthreads();
     if (tid < kRows) {
       const int row = row0 + tid;
       const bool valid = row < n;
@@ -168,36 +185,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (row0 < n) {
-    for (int j = tid; j < nblk; j += kThreads) {
-      bool any = true, all = true;
-      if (p.mask_kind == kMaskCausal) {
-        any = j * BN <= last_row;
-        all = (j + 1) * BN - 1 <= row0;
+    __syncthreads();
+    if (tid == 0) {
+      int ns = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const uint32_t b = steps[j];
+        if (!(b & 1u)) continue;
+        const bool tail = (j + 1) * BN > n || row0 + kRows > n;
+        const uint32_t cls = ((b & 2u) || tail) ? kPartial : kFull;
+        steps[ns++] = static_cast<uint32_t>(j) | (cls << 16);
       }
-      steps[j] = any ? (1u | (all ? 0u : 2u)) : 0u;
+      bars.nsteps = ns;
     }
+  } else if (tid == 0) {
+    bars.nsteps = row0 < n ? (causal ? last_row / BN + 1 : nblk) : 0;
   }
-  __syncthreads();
-  if (tid == 0) {
-    int ns = 0;
-    for (int j = 0; j < nblk; ++j) {
-      const uint32_t b = steps[j];
-      if (!(b & 1u)) continue;
-      const bool tail = (j + 1) * BN > n || row0 + kRows > n;
-      const uint32_t cls = ((b & 2u) || tail) ? kPartial : kFull;
-      steps[ns++] = static_cast<uint32_t>(j) | (cls << 16);
-    }
-    bars.nsteps = ns;
-  }
+  // Step word: key block j | class << 16.
+  auto step_at = [&](int i) -> uint32_t {
+    if (use_table) return steps[i];
+    const bool tail = (i + 1) * BN > n || row0 + kRows > n;
+    const bool full = !tail && (!causal || (i + 1) * BN - 1 <= row0);
+    return static_cast<uint32_t>(i) | ((full ? kFull : kPartial) << 16);
+  };
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const int nsteps = bars.nsteps;
   const uint32_t tmem = bars.tmem_base;
 
-  if (warp == kProducerWarp) {
-    // ---------------------------------------------------------------- TMA producer
+  auto key0_at = [&](int i) { return static_cast<int>(step_at(i) & 0xFFFFu) * BN; };
+  if (warp == kKProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer: Q, dO, K
     if (lane == 0 && nsteps > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -208,21 +226,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sG + b * TQ::kBoxBytes, &tm_g, &bars.qg_full, b * TQ::L::kBoxCols, row0, bh);
       }
       for (int i = 0; i < nsteps; ++i) {
-        const int s = i % NS;
-        const uint32_t ph = (i / NS) & 1;
-        const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
-        if (!mbar_wait_spin(&bars.k_empty[s], ph ^ 1, p.status, 42)) break;
+        const int s = i % NSK;
+        if (!mbar_wait_spin(&bars.k_empty[s], ((i / NSK) & 1) ^ 1, p.status, 42)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], TK::kBytes);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b)
           tma_load_3d(sK + s * TK::kBytes + b * TK::kBoxBytes, &tm_k, &bars.k_full[s],
-                      b * TK::L::kBoxCols, key0, bh);
-        if (!mbar_wait_spin(&bars.v_empty[s], ph ^ 1, p.status, 41)) break;
+                      b * TK::L::kBoxCols, key0_at(i), bh);
+        if (i + kPrefetch < nsteps) {
+          const int kp = key0_at(i + kPrefetch);
+#pragma unroll
+          for (int b = 0; b < TK::L::kBoxes; ++b) {
+            tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, kp, bh);
+            tma_prefetch_l2_3d(&tm_v, b * TK::L::kBoxCols, kp, bh);
+          }
+        }
+      }
+    }
+  } else if (warp == kVProducerWarp) {
+    // ---------------------------------------------------------------- TMA producer: V
+    if (lane == 0) {
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % NSV;
+        if (!mbar_wait_spin(&bars.v_empty[s], ((i / NSV) & 1) ^ 1, p.status, 41)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], TK::kBytes);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b)
           tma_load_3d(sV + s * TK::kBytes + b * TK::kBoxBytes, &tm_v, &bars.v_full[s],
-                      b * TK::L::kBoxCols, key0, bh);
+                      b * TK::L::kBoxCols, key0_at(i), bh);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -238,51 +269,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dkmn0 = TK::desc_mn(smem_u32(sK), 0);
     bool ok = nsteps == 0 || mbar_wait_spin_warp(&bars.qg_full, 0, p.status, 43);
     auto issue_s = [&](int i) -> bool {
-      if (!mbar_wait_spin_warp(&bars.k_full[i % NS], (i / NS) & 1, p.status, 44)) return false;
+      if (!mbar_wait_spin_warp(&bars.k_full[i % NSK], (i / NSK) & 1, p.status, 44)) return false;
       tc_fence_after();
-      const uint64_t dk = dk0 + static_cast<uint64_t>(i % NS) * kStage;
+      const uint64_t dk = dk0 + static_cast<uint64_t>(i % NSK) * kStage;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS + (i & 1) * BN, dq0 + TQ::k_step(kk), dk + TK::k_step(kk), id_s,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(&bars.s_full[i & 1]);
+          mma_ss(tmem + C::kColS, dq0 + TQ::k_step(kk), dk + TK::k_step(kk), id_s, kk > 0 ? 1u : 0u);
+        mma_commit(&bars.s_full);
       }
       __syncwarp();
       return true;
     };
     auto issue_dp = [&](int i) -> bool {
-      if (!mbar_wait_spin_warp(&bars.v_full[i % NS], (i / NS) & 1, p.status, 45)) return false;
+      if (!mbar_wait_spin_warp(&bars.v_full[i % NSV], (i / NSV) & 1, p.status, 45)) return false;
       tc_fence_after();
-      const uint64_t dv = dv0 + static_cast<uint64_t>(i % NS) * kStage;
+      const uint64_t dv = dv0 + static_cast<uint64_t>(i % NSV) * kStage;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, dg0 + TQ::k_step(kk), dv + TK::k_step(kk), id_s, kk > 0 ? 1u : 0u);
-        mma_commit(&bars.dp_full);
-        mma_commit(&bars.v_empty[i % NS]);
+          mma_ss(tmem + C::kColDP + (i & 1) * BN, dg0 + TQ::k_step(kk), dv + TK::k_step(kk), id_s,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&bars.dp_full[i & 1]);
+        mma_commit(&bars.v_empty[i % NSV]);
       }
       __syncwarp();
       return true;
     };
     if (ok && nsteps > 0) ok = issue_s(0) && issue_dp(0);
     for (int i = 0; i < nsteps && ok; ++i) {
-      const bool more = i + 1 < nsteps;
-      if (more) ok = issue_s(i + 1);
-      if (!ok) break;
+      if (i + 1 < nsteps) {
+        // S_{i+1} overwrites S_i: wait until every softmax warp has loaded it
+        ok = mbar_wait_spin_warp(&bars.s_free, i & 1, p.status, 50);
+        if (!ok) break;
+        tc_fence_after();
+        ok = issue_s(i + 1) && issue_dp(i + 1);
+        if (!ok) break;
+      }
       ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 46);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t dkmn = dkmn0 + static_cast<uint64_t>(i % NS) * kStage;
+      const uint64_t dkmn = dkmn0 + static_cast<uint64_t>(i % NSK) * kStage;
+      const uint32_t ds_col = C::kColDP + (i & 1) * BN;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(16 * kk), dkmn + TK::mn_step(kk),
+          mma_ts(tmem + C::kColDQ, tmem + ds_col + packed_col(16 * kk), dkmn + TK::mn_step(kk),
                  id_q, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.k_empty[i % NS]);
+        mma_commit(&bars.k_empty[i % NSK]);
       }
       __syncwarp();
-      if (more) ok = issue_dp(i + 1);
     }
     if (elect_one()) mma_commit(&bars.dq_done);
     __syncwarp();
@@ -335,11 +371,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
                   static_cast<int64_t>(row < n ? row : 0) * p.mask_row_words
             : nullptr;
-    const uint32_t tP = tmem + C::kColDP + lane_off;
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
-      const int key0 = static_cast<int>(steps[i] & 0xFFFFu) * BN;
-      const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
+      const uint32_t sw = step_at(i);
+      const int key0 = static_cast<int>(sw & 0xFFFFu) * BN;
+      const bool partial = ((sw >> 16) & 3u) == kPartial;
       uint32_t mword[kHalf / 32];
       if (partial && p.mask_kind == kMaskBitmap) {
 #pragma unroll
@@ -351,16 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mword[q] = w;
         }
       }
-      ok = mbar_wait_spin(&bars.s_full[i & 1], (i >> 1) & 1, p.status, 47);
+      ok = mbar_wait_spin(&bars.s_full, i & 1, p.status, 47);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem + C::kColS + (i & 1) * BN + lane_off;
+      const uint32_t tS = tmem + C::kColS + lane_off;
+      const uint32_t tP = tmem + C::kColDP + (i & 1) * BN + lane_off;
       uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
       // both 32-column chunks are loaded before one wait: the load latency is paid once
       uint32_t rr[kHalf / 32][32];
 #pragma unroll
       for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tS + c_lo + 32 * h, rr[h]);
       tmem_wait_ld();
+      // S is in registers: the tensor core may overwrite it with S_{i+1}
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_free);
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
@@ -385,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k) pkeep[cc / 2 + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
       }
-      ok = mbar_wait_spin(&bars.dp_full, i & 1, p.status, 48);
+      ok = mbar_wait_spin(&bars.dp_full[i & 1], (i >> 1) & 1, p.status, 48);
       if (!ok) break;
       tc_fence_after();
       uint32_t dp[kHalf / 32][32];
@@ -410,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ds_full);
     }
-    // ---------------------------------------------------------------- epilogue (warps 1-4)
+    // ---------------------------------------------------------------- epilogue (warps 3-6)
     // dQ = c * (dS K) rounded and stored through the (now idle) Q tile.
     if (half == 0 && row0 < n) {
       if (ok && nsteps > 0) ok = mbar_wait_spin(&bars.dq_done, 0, p.status, 49);
