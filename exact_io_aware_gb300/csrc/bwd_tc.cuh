@@ -128,6 +128,19 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// 32 consecutive floats of shared memory (16-byte aligned) with eight 16-byte loads.
+__device__ __forceinline__ void load32(const float* src, float (&dst)[32]) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const float4 t = s4[v];
+    dst[4 * v] = t.x;
+    dst[4 * v + 1] = t.y;
+    dst[4 * v + 2] = t.z;
+    dst[4 * v + 3] = t.w;
+  }
+}
+
 template <bool kBf16>
 __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   if constexpr (kBf16) {
@@ -416,7 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c0 = c_lo + cc;
         float pv[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[cc / 32][k]) * sl2 - L[c0 + k]);
+        // The block's LSE values are the same for every lane: 16-byte loads take a quarter of
+        // the shared-memory cycles of scalar ones, cycles the products' operand reads need.
+        float lv[32];
+        load32(L + c0, lv);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[cc / 32][k]) * sl2 - lv[k]);
         // Masking is a separate pass over the chunk so the common (full-block) path above
         // stays one compact run of instructions.
         if (partial) {
@@ -459,12 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
         uint32_t pk[16];
+        float dv[32];
+        load32(Dd + c0, dv);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
           unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
-          const float g0 = p0 * (__uint_as_float(dp[cc / 32][2 * k]) - Dd[c0 + 2 * k]);
-          const float g1 = p1 * (__uint_as_float(dp[cc / 32][2 * k + 1]) - Dd[c0 + 2 * k + 1]);
+          const float g0 = p0 * (__uint_as_float(dp[cc / 32][2 * k]) - dv[2 * k]);
+          const float g1 = p1 * (__uint_as_float(dp[cc / 32][2 * k + 1]) - dv[2 * k + 1]);
           pk[k] = pack2<kBf16>(g0, g1);
         }
         tmem_st16(tP + packed_col(c0), pk);
