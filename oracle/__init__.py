@@ -9,10 +9,12 @@ the pages on exact IO-aware attention:
 * ``masks``      — allowed-key sets: none, causal, and the packed bitmap the library reads.
 * ``io_model``   — a global-memory byte counter for the unfused and fused kernels of the
                    "Night School: fused attention" lab.
+* ``dropout``    — the dropout extension with a replayed realised mask (Philox4x32-10 mask,
+                   forward and reverse pass with the mask held fixed).
 
 Only the test suite, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg may import
 this package.  The GPU library never does, and this package imports nothing from it.
 Every function here is pinned by ``-m "not gpu"`` tests against worked examples, closed
 forms, invariants or brute force; none is marked "parity unpinned".
 """
-from . import attention, io_model, masks, tiled  # noqa: F401
+from . import attention, dropout, io_model, masks, tiled  # noqa: F401

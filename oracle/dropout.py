@@ -1,0 +1,98 @@
+"""Dropout on the attention probabilities with a replayed realised mask, in float64 (test
+infrastructure only).
+
+The pages' base procedure has no dropout and require of any dropout extension that its
+reverse pass reuse the realised mask of the forward ("Exact tiled attention and
+memory-aware differentiation", the reverse procedure and the closing remark on rounding):
+a different mask differentiates a different function.  The library's reading, which this
+module restates:
+
+* Mask.  For head index bh (b·H + h), query row i and key j, the generator is
+  Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+  1, 2, 3", SC 2011): counter (i, ⌊j/4⌋, bh, 0), key (seed mod 2^32, ⌊seed / 2^32⌋).  Word
+  j mod 4 of the output is compared with the integer threshold t = round(p·2^32): the
+  pair (i, j) is kept iff word ≥ t.  Integer arithmetic end to end, so the mask is the same
+  bit for bit wherever it is drawn.
+* Forward.  P_ij = exp(s_ij − LSE_i) as without dropout (LSE is not changed by dropout);
+  O_i = Σ_j P_ij M_ij V_j / (1 − p).
+* Reverse, for upstream G: with P̃ = P∘M/(1 − p), dV = P̃ᵀ G;  dP̃_ij = G_i·V_j;
+  D_i = G_i·O_i (= Σ_j P̃_ij dP̃_ij);  dS_ij = P_ij (M_ij dP̃_ij/(1 − p) − D_i);
+  dQ = c·dS K, dK = c·dSᵀ Q.  This is the chain rule through O = (P∘M/(1−p)) V and the
+  softmax, the mask held fixed.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# Philox4x32 constants of the publication: round multipliers and the key's Weyl increments.
+_M0, _M1 = 0xD2511F53, 0xCD9E8D57
+_W0, _W1 = 0x9E3779B9, 0xBB67AE85
+_MASK32 = 0xFFFFFFFF
+
+
+def philox4x32(ctr, key, rounds=10):
+    """Philox4x32 with ``rounds`` rounds.  ``ctr``: uint32 array [..., 4]; ``key``: two ints.
+    Returns uint32 [..., 4]."""
+    c = np.asarray(ctr, dtype=np.uint64) & _MASK32
+    c0, c1, c2, c3 = (c[..., t].copy() for t in range(4))
+    k0, k1 = int(key[0]) & _MASK32, int(key[1]) & _MASK32
+    for r in range(rounds):
+        if r:
+            k0, k1 = (k0 + _W0) & _MASK32, (k1 + _W1) & _MASK32
+        p0 = c0 * np.uint64(_M0)  # exact: both factors < 2^32
+        p1 = c2 * np.uint64(_M1)
+        hi0, lo0 = p0 >> np.uint64(32), p0 & np.uint64(_MASK32)
+        hi1, lo1 = p1 >> np.uint64(32), p1 & np.uint64(_MASK32)
+        c0, c1, c2, c3 = (hi1 ^ c1 ^ np.uint64(k0), lo1, hi0 ^ c3 ^ np.uint64(k1), lo0)
+    return np.stack([c0, c1, c2, c3], axis=-1).astype(np.uint32)
+
+
+def threshold(p):
+    """Integer drop threshold round(p·2^32) for a drop probability 0 <= p < 1."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("drop probability must be in [0, 1)")
+    return int(round(p * 2.0 ** 32))
+
+
+def keep_mask(seed, bh, rows, n, p):
+    """Kept pairs of head ``bh`` for query ``rows`` and keys 0..n-1: bool [len(rows), n]."""
+    rows = np.asarray(rows, dtype=np.int64)
+    ctr = np.zeros((rows.size, (n + 3) // 4, 4), dtype=np.uint64)
+    ctr[..., 0] = rows[:, None]
+    ctr[..., 1] = np.arange((n + 3) // 4)[None, :]
+    ctr[..., 2] = bh
+    words = philox4x32(ctr, (seed & _MASK32, (seed >> 32) & _MASK32)).reshape(rows.size, -1)[:, :n]
+    return words.astype(np.uint64) >= np.uint64(threshold(p))
+
+
+def forward_rows(q, k, v, c, allowed, keep, p):
+    """O, LSE of one head's query rows ``q`` under dropout with kept pairs ``keep``."""
+    q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
+    s = np.where(allowed, float(c) * (q @ k.T), -np.inf)
+    m = s.max(axis=1)
+    nonempty = np.isfinite(m)
+    e = np.exp(s - np.where(nonempty, m, 0.0)[:, None])
+    ell = e.sum(axis=1)
+    safe = np.where(nonempty, ell, 1.0)
+    P = e / safe[:, None]
+    y = ((P * keep) @ v) / (1.0 - p)
+    y[~nonempty] = 0.0
+    lse = np.where(nonempty, m + np.log(safe), -np.inf)
+    return y, lse
+
+
+def backward_head(q, k, v, c, allowed, keep, p, G):
+    """dQ, dK, dV of one head under dropout (the mask ``keep`` replayed)."""
+    q, k, v, G = (np.asarray(x, dtype=np.float64) for x in (q, k, v, G))
+    y, lse = forward_rows(q, k, v, c, allowed, keep, p)
+    s = np.where(allowed, float(c) * (q @ k.T), -np.inf)
+    fin = np.isfinite(lse)
+    P = np.where(fin[:, None], np.exp(s - np.where(fin, lse, 0.0)[:, None]), 0.0)
+    Pt = P * keep / (1.0 - p)
+    dV = Pt.T @ G
+    dPt = G @ v.T
+    D = (G * y).sum(axis=1)
+    dS = P * (keep * dPt / (1.0 - p) - D[:, None])
+    dQ = float(c) * dS @ k
+    dK = float(c) * dS.T @ q
+    return dQ, dK, dV
