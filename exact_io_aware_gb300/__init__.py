@@ -18,6 +18,7 @@ import os
 import torch
 
 __all__ = [
+    "attn_fwd_dropout", "attn_bwd_dropout",
     "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
@@ -25,6 +26,7 @@ __all__ = [
     "attn_selftest_wait_timeout", "attn_fwd_split", "attn_fwd_split_count",
     "attn_fwd_split_workspace_bytes", "attn_merge",
 ]
+
 
 ATTN_OK = 0
 ATTN_WARN_EMPTY_ROW = 1
@@ -82,6 +84,13 @@ def load():
     lib.attn_fwd_split_workspace_bytes.restype = sz
     lib.attn_merge.argtypes = [i32, i32, i64, i32, vp, vp, vp, vp, vp]
     lib.attn_merge.restype = i32
+    u64 = ctypes.c_uint64
+    lib.attn_fwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
+                                     i32, f32, u64, vp, vp, vp]
+    lib.attn_fwd_dropout.restype = i32
+    lib.attn_bwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, i32,
+                                     vp, i64, i64, i32, f32, u64, vp, vp, vp, vp, sz, vp]
+    lib.attn_bwd_dropout.restype = i32
     _lib = lib
     return lib
 
@@ -131,17 +140,25 @@ def _mask_args(mask, mask_bits, mask_head_stride_words):
 
 
 def attn_fwd(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=0, kv_block=0,
-             o=None, lse=None, stream=None):
-    """Forward pass; returns (o [B,H,n,d], lse [B,H,n] float32)."""
+             o=None, lse=None, stream=None, dropout_p=0.0, seed=0):
+    """Forward pass; returns (o [B,H,n,d], lse [B,H,n] float32).  dropout_p > 0 drops
+    probabilities with the library's replayable mask for ``seed`` (attn_fwd_dropout)."""
     B, H, n, d = _shape(q, k, v)
     kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
-    _check(load().attn_fwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
-                           kind, _ptr(bits), row_words, hs, int(kv_block), _ptr(o), _ptr(lse),
-                           _stream_ptr(stream)))
+    lib = load()
+    if dropout_p:
+        _check(lib.attn_fwd_dropout(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k),
+                                    _ptr(v), kind, _ptr(bits), row_words, hs, int(kv_block),
+                                    float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(o),
+                                    _ptr(lse), _stream_ptr(stream)))
+        return o, lse
+    _check(lib.attn_fwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
+                        kind, _ptr(bits), row_words, hs, int(kv_block), _ptr(o), _ptr(lse),
+                        _stream_ptr(stream)))
     return o, lse
 
 
@@ -198,14 +215,30 @@ def attn_merge(o_parts, lse_parts, dtype=torch.float32, o=None, lse=None, stream
     return o, lse
 
 
+def attn_fwd_dropout(q, k, v, c, dropout_p, seed, **kw):
+    """attn_fwd with dropout: the C entry point of the same name (see attn_fwd)."""
+    if not dropout_p:
+        raise ValueError("attn_fwd_dropout needs dropout_p > 0 (use attn_fwd otherwise)")
+    return attn_fwd(q, k, v, c, dropout_p=dropout_p, seed=seed, **kw)
+
+
+def attn_bwd_dropout(q, k, v, o, lse, do, c, dropout_p, seed, **kw):
+    """attn_bwd replaying the dropout mask of attn_fwd_dropout for the same seed."""
+    if not dropout_p:
+        raise ValueError("attn_bwd_dropout needs dropout_p > 0 (use attn_bwd otherwise)")
+    return attn_bwd(q, k, v, o, lse, do, c, dropout_p=dropout_p, seed=seed, **kw)
+
+
 def attn_bwd_workspace_bytes(dtype, B, H, n, d) -> int:
     code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return int(load().attn_bwd_workspace_bytes(code, B, H, n, d))
 
 
 def attn_bwd(q, k, v, o, lse, do, c, mask="none", mask_bits=None, mask_head_stride_words=0,
-             kv_block=0, dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Backward pass (vector-Jacobian product for upstream ``do``); returns (dq, dk, dv)."""
+             kv_block=0, dq=None, dk=None, dv=None, workspace=None, stream=None, dropout_p=0.0,
+             seed=0):
+    """Backward pass (vector-Jacobian product for upstream ``do``); returns (dq, dk, dv).
+    dropout_p and seed must be those of the forward (attn_bwd_dropout replays its mask)."""
     B, H, n, d = _shape(q, k, v)
     kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
     dq = torch.empty_like(q) if dq is None else dq
@@ -214,10 +247,19 @@ def attn_bwd(q, k, v, o, lse, do, c, mask="none", mask_bits=None, mask_head_stri
     need = attn_bwd_workspace_bytes(q.dtype, B, H, n, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check(load().attn_bwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
-                           _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits), row_words, hs,
-                           int(kv_block), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-                           workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    lib = load()
+    if dropout_p:
+        _check(lib.attn_bwd_dropout(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k),
+                                    _ptr(v), _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits),
+                                    row_words, hs, int(kv_block), float(dropout_p),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dq), _ptr(dk), _ptr(dv),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream_ptr(stream)))
+        return dq, dk, dv
+    _check(lib.attn_bwd(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k), _ptr(v),
+                        _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits), row_words, hs,
+                        int(kv_block), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return dq, dk, dv
 
 
@@ -266,20 +308,22 @@ def attn_device_status(stream=None) -> int:
 
 class _Attention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, c, mask, mask_bits, kv_block):
-        o, lse = attn_fwd(q, k, v, c, mask, mask_bits, 0, kv_block)
+    def forward(ctx, q, k, v, c, mask, mask_bits, kv_block, dropout_p, seed):
+        o, lse = attn_fwd(q, k, v, c, mask, mask_bits, 0, kv_block, dropout_p=dropout_p,
+                          seed=seed)
         ctx.save_for_backward(q, k, v, o, lse, mask_bits)
-        ctx.c, ctx.mask, ctx.kv_block = c, mask, kv_block
+        ctx.c, ctx.mask, ctx.kv_block, ctx.dropout_p, ctx.seed = c, mask, kv_block, dropout_p, seed
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse, mask_bits = ctx.saved_tensors
         dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), ctx.c, ctx.mask, mask_bits, 0,
-                              ctx.kv_block)
-        return dq, dk, dv, None, None, None, None
+                              ctx.kv_block, dropout_p=ctx.dropout_p, seed=ctx.seed)
+        return dq, dk, dv, None, None, None, None, None, None
 
 
-def attention(q, k, v, c, mask="none", mask_bits=None, kv_block=0):
-    """Differentiable exact attention O = softmax(c QKᵀ + mask) V."""
-    return _Attention.apply(q, k, v, c, mask, mask_bits, kv_block)
+def attention(q, k, v, c, mask="none", mask_bits=None, kv_block=0, dropout_p=0.0, seed=0):
+    """Differentiable exact attention O = softmax(c QKᵀ + mask) V, with optional dropout on
+    the probabilities (the backward replays the forward's mask for ``seed``)."""
+    return _Attention.apply(q, k, v, c, mask, mask_bits, kv_block, dropout_p, seed)

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <string>
@@ -145,9 +146,26 @@ void ea::set_last_error(const std::string& msg) { g_last_error = msg; }
 
 extern "C" {
 
-int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+}  // extern "C"
+
+namespace {
+
+// Dropout arguments of a call: p in [0, 1); threshold floor(p 2^32 + 1/2), scale 1/(1-p).
+int set_dropout(float p_drop, uint64_t seed, ea::AttnArgs& a) {
+  if (!(p_drop >= 0.0f && p_drop < 1.0f))
+    return fail(ATTN_ERR_INVALID_ARG, "p_drop must lie in [0, 1)");
+  a.dropout = p_drop > 0.0f;
+  a.drop.thr = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 4294967296.0 + 0.5));
+  a.drop.scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  a.drop.seed_lo = static_cast<uint32_t>(seed);
+  a.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
+  return ATTN_OK;
+}
+
+int fwd_impl(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
              const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
-             int64_t mask_head_stride_words, int kv_block, void* o, float* lse, void* stream) {
+             int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed, void* o,
+             float* lse, void* stream) {
   if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
                             mask_head_stride_words, kv_block))
     return rc;
@@ -159,6 +177,7 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
                              mask_head_stride_words, kv_block);
   a.o_out = o;
   a.lse = lse;
+  if (int rc = set_dropout(p_drop, seed, a)) return rc;
   if (int rc = status_ptr(&a.status)) return rc;
   std::string err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -166,6 +185,25 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
                              : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
   if (rc) return fail(rc, err);
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+             const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+             int64_t mask_head_stride_words, int kv_block, void* o, float* lse, void* stream) {
+  return fwd_impl(dtype, B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                  mask_head_stride_words, kv_block, 0.0f, 0, o, lse, stream);
+}
+
+int attn_fwd_dropout(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+                     const void* v, int mask_kind, const uint32_t* mask_bits,
+                     int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
+                     float p_drop, uint64_t seed, void* o, float* lse, void* stream) {
+  return fwd_impl(dtype, B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                  mask_head_stride_words, kv_block, p_drop, seed, o, lse, stream);
 }
 
 int attn_fwd_split_count(int dtype, int B, int H, int n, int d, int kv_block) {
@@ -248,11 +286,15 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int n, int d) {
                            : ea::bwd_tc_workspace_bytes(B, H, n, d);
 }
 
-int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+}  // extern "C"
+
+namespace {
+
+int bwd_impl(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
              const void* v, const void* o, const float* lse, const void* d_o, int mask_kind,
              const uint32_t* mask_bits, int64_t mask_row_words, int64_t mask_head_stride_words,
-             int kv_block, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-             void* stream) {
+             int kv_block, float p_drop, uint64_t seed, void* dq, void* dk, void* dv,
+             void* workspace, size_t workspace_bytes, void* stream) {
   if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
                             mask_head_stride_words, kv_block))
     return rc;
@@ -276,6 +318,7 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
   a.dv = dv;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
+  if (int rc = set_dropout(p_drop, seed, a)) return rc;
   if (int rc = status_ptr(&a.status)) return rc;
   std::string err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -283,6 +326,31 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
                              : ea::launch_bwd_tc(dtype == ATTN_BF16, a, s, err);
   if (rc) return fail(rc, err);
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+             const void* v, const void* o, const float* lse, const void* d_o, int mask_kind,
+             const uint32_t* mask_bits, int64_t mask_row_words, int64_t mask_head_stride_words,
+             int kv_block, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+             void* stream) {
+  return bwd_impl(dtype, B, H, n, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
+                  mask_row_words, mask_head_stride_words, kv_block, 0.0f, 0, dq, dk, dv,
+                  workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_dropout(int dtype, int B, int H, int n, int d, float c, const void* q,
+                     const void* k, const void* v, const void* o, const float* lse,
+                     const void* d_o, int mask_kind, const uint32_t* mask_bits,
+                     int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
+                     float p_drop, uint64_t seed, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return bwd_impl(dtype, B, H, n, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
+                  mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, dq, dk, dv,
+                  workspace, workspace_bytes, stream);
 }
 
 int attn_device_status(void* stream) {

@@ -27,6 +27,9 @@
 //   warp  9    TMA producer (K, V once; Q, dO, LSE, D per block through an NS-stage ring)
 // Issue order per block i: dV_i, S_{i+1}, dK_i, dP_{i+1}: S_{i+1} follows dV_i, the last reader
 // of P_i, and dP_{i+1} follows dK_i, the last reader of dS_i.
+// Dropout (kDrop): the mask of dropout.cuh is redrawn for the block's (query, key) pairs; the
+// dV operand is P with dropped pairs zeroed (dV is scaled by 1/(1-p) in the epilogue), and
+// dS = P (keep ? dP/(1-p) : 0) - P D uses the unzeroed P.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -64,6 +67,7 @@ struct BwdParams {
   const void* o;
   const void* d_o;
   uint32_t* status;
+  DropoutArgs drop;  // read only by the dropout instantiations
 };
 
 __host__ __device__ constexpr int pad32(int x) { return x < 32 ? 32 : x; }
@@ -154,7 +158,7 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   }
 }
 
-template <bool kBf16, int D>
+template <bool kBf16, int D, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -415,6 +419,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* Dd = sD + (i % NS) * BQ;
       ok = mbar_wait_spin(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
       if (!ok) break;
+      // Dropout: keep bits of this key with the warp's query columns (bit k of word h <->
+      // query q0 + c_lo + 32 h + k), drawn while the scores are still being computed.
+      uint32_t kbits[kDrop ? kHalf / 32 : 1];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int h = 0; h < kHalf / 32; ++h) {
+          uint32_t w = 0;
+#pragma unroll 1
+          for (int k = 0; k < 32; ++k)
+            w |= (keep1(p.drop, static_cast<uint32_t>(q0 + c_lo + 32 * h + k),
+                        static_cast<uint32_t>(j), bh) ? 1u : 0u) << k;
+          kbits[h] = w;
+        }
+      }
       ok = mbar_wait_spin(&bars.s_full, i & 1, p.status, 27);
       if (!ok) break;
       tc_fence_after();
@@ -428,7 +446,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < kHalf; cc += 32) {
         const int c0 = c_lo + cc;
         float pv[32];
-#pragma unroll
         // The block's LSE values are the same for every lane: 16-byte loads take a quarter of
         // the shared-memory cycles of scalar ones, cycles the products' operand reads need.
         float lv[32];
@@ -456,8 +473,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          pk[k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
-          pkeep[cc / 2 + k] = pk[k];
+          pkeep[cc / 2 + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
+          if constexpr (kDrop) {
+            const uint32_t kb = kbits[cc / 32] >> (2 * k);
+            pk[k] = pack2<kBf16>(kb & 1u ? pv[2 * k] : 0.0f, kb & 2u ? pv[2 * k + 1] : 0.0f);
+          } else {
+            pk[k] = pkeep[cc / 2 + k];
+          }
         }
         tmem_st16(tS + packed_col(c0), pk);
       }
@@ -483,8 +505,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
           unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
-          const float g0 = p0 * (__uint_as_float(dp[cc / 32][2 * k]) - dv[2 * k]);
-          const float g1 = p1 * (__uint_as_float(dp[cc / 32][2 * k + 1]) - dv[2 * k + 1]);
+          float d0 = __uint_as_float(dp[cc / 32][2 * k]);
+          float d1 = __uint_as_float(dp[cc / 32][2 * k + 1]);
+          if constexpr (kDrop) {
+            const uint32_t kb = kbits[cc / 32] >> (2 * k);
+            d0 = kb & 1u ? d0 * p.drop.scale : 0.0f;
+            d1 = kb & 2u ? d1 * p.drop.scale : 0.0f;
+          }
+          const float g0 = p0 * (d0 - dv[2 * k]);
+          const float g1 = p1 * (d1 - dv[2 * k + 1]);
           pk[k] = pack2<kBf16>(g0, g1);
         }
         tmem_st16(tP + packed_col(c0), pk);
@@ -497,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- epilogue (warps 1-4)
     // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
     if (half == 0) {
+      const float dvs = kDrop ? p.drop.scale : 1.0f;  // dV = (P with dropped pairs zeroed)ᵀ dO / (1-p)
       if (ok) ok = mbar_wait_spin(&bars.kv_done, 0, p.status, 31);
       tc_fence_after();
       if (ok) {
@@ -514,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pv[8], pkk[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            pv[k] = pack2<kBf16>(__uint_as_float(rv[2 * k]), __uint_as_float(rv[2 * k + 1]));
+            pv[k] = pack2<kBf16>(dvs * __uint_as_float(rv[2 * k]), dvs * __uint_as_float(rv[2 * k + 1]));
             pkk[k] = pack2<kBf16>(p.c * __uint_as_float(rk[2 * k]), p.c * __uint_as_float(rk[2 * k + 1]));
           }
           *reinterpret_cast<uint4*>(sV + TK::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);

@@ -3,6 +3,6 @@
 
 namespace ea {
 int launch_bwd_tc_d16(bool bf16, const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
-  return bf16 ? bwd::run<true, 16>(a, table, s, err) : bwd::run<false, 16>(a, table, s, err);
+  return bwd::run_d<16>(bf16, a, table, s, err);
 }
 }  // namespace ea

@@ -10,7 +10,7 @@ namespace bwd {
 
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 
-template <bool kBf16, int D>
+template <bool kBf16, int D, bool kDrop>
 int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   using Cfg = Config<D>;
   using QCfg = dq::Config<D>;
@@ -38,9 +38,10 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   float* L2 = table;
   BwdParams p{a.n,  a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
               L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.status};
+  p.drop = a.drop;
   const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
   // the dQ kernel writes the row table the dK/dV kernel reads
-  auto qkern = dq::dq_tc_kernel<kBf16, D>;
+  auto qkern = dq::dq_tc_kernel<kBf16, D, kDrop>;
   cudaError_t e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(qsmem));
   if (e == cudaSuccess) {
@@ -51,7 +52,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
     err = std::string("dQ launch: ") + cudaGetErrorString(e);
     return -5;
   }
-  auto kern = bwd_tc_kernel<kBf16, D>;
+  auto kern = bwd_tc_kernel<kBf16, D, kDrop>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e == cudaSuccess) {
@@ -63,6 +64,14 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
     return -5;
   }
   return 0;
+}
+
+// Instantiations with and without dropout for one head dimension.
+template <int D>
+int run_d(bool bf16, const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
+  if (a.dropout)
+    return bf16 ? run<true, D, true>(a, table, s, err) : run<false, D, true>(a, table, s, err);
+  return bf16 ? run<true, D, false>(a, table, s, err) : run<false, D, false>(a, table, s, err);
 }
 
 }  // namespace bwd

@@ -18,6 +18,8 @@
 //   dP = dO V_jᵀ          (two buffers, so dP_{j+1} is computed while dQ_j reads dS_j)
 //   dS = P (dP - D)                      softmax warps; 16-bit, written over dP
 //   dQ += dS K_j                         (A operand read from tensor memory)
+// Dropout (kDrop): dS = P (keep ? dP/(1-p) : 0) - P D with the mask of dropout.cuh redrawn for
+// the block's (query, key) pairs; P itself is not masked here (dQ needs only dS).
 // Roles (the control warps take the lowest warp slots, which the warp schedulers favour over
 // the softmax warps they share a sub-partition with):
 //   warp  0    TMEM allocator and MMA issuer
@@ -97,7 +99,7 @@ struct Barriers {
   float dpart[2][kRows];  // per-row partial sums of dO * O over each half of the columns
 };
 
-template <bool kBf16, int D>
+template <bool kBf16, int D, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -426,6 +428,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 16; ++k) pkeep[cc / 2 + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
       }
+      // Dropout: keep bits of this row with the warp's key columns (bit k of word h <-> key
+      // key0 + c_lo + 32 h + k), drawn before the wait for dP.
+      uint32_t kbits[kDrop ? kHalf / 32 : 1];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int h = 0; h < kHalf / 32; ++h) {
+          uint32_t w = 0;
+#pragma unroll 1
+          for (int g = 0; g < 8; ++g)
+            w |= keep4(p.drop, static_cast<uint32_t>(row),
+                       static_cast<uint32_t>(key0 + c_lo + 32 * h + 4 * g) >> 2, bh) << (4 * g);
+          kbits[h] = w;
+        }
+      }
       ok = mbar_wait_spin(&bars.dp_full[i & 1], (i >> 1) & 1, p.status, 48);
       if (!ok) break;
       tc_fence_after();
@@ -441,8 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
           unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
-          pk[k] = pack2<kBf16>(p0 * (__uint_as_float(dp[cc / 32][2 * k]) - dd),
-                               p1 * (__uint_as_float(dp[cc / 32][2 * k + 1]) - dd));
+          float d0 = __uint_as_float(dp[cc / 32][2 * k]);
+          float d1 = __uint_as_float(dp[cc / 32][2 * k + 1]);
+          if constexpr (kDrop) {
+            const uint32_t kb = kbits[cc / 32] >> (2 * k);
+            d0 = kb & 1u ? d0 * p.drop.scale : 0.0f;
+            d1 = kb & 2u ? d1 * p.drop.scale : 0.0f;
+          }
+          pk[k] = pack2<kBf16>(p0 * (d0 - dd), p1 * (d1 - dd));
         }
         tmem_st16(tP + packed_col(c0), pk);
       }

@@ -27,6 +27,10 @@
 // O_z = z/l (float32) and LSE_z = m + ln l (-inf for a row with no allowed key in the share),
 // which a merge kernel combines by the merge rule of the stable summaries.
 //
+// Dropout (kDrop): the realised mask of dropout.cuh zeroes dropped probabilities on their way
+// into P (the row sum l keeps every probability), and the factor 1/(1-p) is applied to O in
+// the epilogue, so the 16-bit P never exceeds the range it has without dropout.
+//
 // Online softmax (the running-maximum recurrence of "The Arithmetic of Intelligence",
 // chapter 12): scores are taken to base 2 with the folded factor c·log2(e) (the exp2
 // prescale described in "Bellek Duvarının Fiziği", online softmax section).  The running
@@ -130,7 +134,7 @@ __device__ __forceinline__ uint32_t dense_step(int j, int BN, int nblk, int n, i
   return w;
 }
 
-template <bool kBf16, int D, int BN>
+template <bool kBf16, int D, int BN, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -422,6 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t cls = (sw >> (16 + 2 * t)) & 3u;
       if (cls == kSkip) continue;
       const int key0 = static_cast<int>(sw & 0xFFFFu) * BN;
+      // Dropout: the block's keep bits (bit k of word q <-> key key0 + 32 q + k) are drawn
+      // while the scores are still being computed; the exponential loop only tests them.
+      uint32_t kbits[kDrop ? BN / 32 : 1];
+      if constexpr (kDrop) {
+#pragma unroll
+        for (int q = 0; q < BN / 32; ++q) {
+          uint32_t w = 0;
+#pragma unroll 1
+          for (int g = 0; g < 8; ++g)
+            w |= keep4(p.drop, static_cast<uint32_t>(row),
+                       static_cast<uint32_t>(key0 + 32 * q + 4 * g) >> 2, bh) << (4 * g);
+          kbits[q] = w;
+        }
+      }
       ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
       if (!ok) break;
       s_phase ^= 1;
@@ -525,8 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           r1 += p1;
           r2 += p2;
           r3 += p3;
-          pk[k] = pack2<kBf16>(p0, p1);
-          pk[k + 1] = pack2<kBf16>(p2, p3);
+          if constexpr (kDrop) {
+            const uint32_t kb = kbits[c0 / 32] >> (2 * k);  // keys c0 + 2k .. c0 + 2k + 3
+            pk[k] = pack2<kBf16>(kb & 1u ? p0 : 0.0f, kb & 2u ? p1 : 0.0f);
+            pk[k + 1] = pack2<kBf16>(kb & 4u ? p2 : 0.0f, kb & 8u ? p3 : 0.0f);
+          } else {
+            pk[k] = pack2<kBf16>(p0, p1);
+            pk[k + 1] = pack2<kBf16>(p2, p3);
+          }
         }
         tmem_st16(tS + lane_off + c0 / 2, pk);
       }
@@ -544,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pair_row0 + t * kRowsPerTile < n) {
         if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
         tc_fence_after();
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        const float inv = l > 0.0f ? (kDrop ? p.drop.scale : 1.0f) / l : 0.0f;
         // The TMEM loads are warp-collective: every lane takes part, rows past n included;
         // only the stores are per row.
         if (ok) {
@@ -577,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and -inf, like any other row with an empty allowed set.
       if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
       tc_fence_after();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      const float inv = l > 0.0f ? (kDrop ? p.drop.scale : 1.0f) / l : 0.0f;
       uint8_t* stage = sQ + t * TQ::kBytes;  // Q_t is dead once every MMA of tile t is done
       if (ok) {
 #pragma unroll

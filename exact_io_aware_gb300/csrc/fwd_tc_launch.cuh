@@ -9,7 +9,7 @@
 namespace ea {
 namespace fwd {
 
-template <bool kBf16, int D, int BN>
+template <bool kBf16, int D, int BN, bool kDrop>
 int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   using Cfg = Config<D, BN>;
   const size_t smem = Cfg::smem_bytes(a.n, a.mask_kind);
@@ -28,7 +28,7 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
     err = "cuTensorMapEncodeTiled rejected a forward tensor map";
     return -5;
   }
-  auto kern = fwd_tc_kernel<kBf16, D, BN>;
+  auto kern = fwd_tc_kernel<kBf16, D, BN, kDrop>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
@@ -38,7 +38,7 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   const int nsplit = a.num_splits > 1 ? a.num_splits : 1;
   FwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
               a.lse, a.status, nsplit, nsplit > 1 ? a.o_part : nullptr,
-              nsplit > 1 ? a.lse_part : nullptr};
+              nsplit > 1 ? a.lse_part : nullptr, a.drop};
   dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads),
             static_cast<unsigned>(nsplit));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);
@@ -50,15 +50,21 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   return 0;
 }
 
-template <int D>
-int launch_d(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
+template <int D, bool kDrop>
+int launch_dd(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
   const int bn = a.kv_block == 0 ? 128 : a.kv_block;
   switch (bn) {
-    case 32: return bf16 ? run<true, D, 32>(a, s, err) : run<false, D, 32>(a, s, err);
-    case 64: return bf16 ? run<true, D, 64>(a, s, err) : run<false, D, 64>(a, s, err);
-    case 128: return bf16 ? run<true, D, 128>(a, s, err) : run<false, D, 128>(a, s, err);
+    case 32: return bf16 ? run<true, D, 32, kDrop>(a, s, err) : run<false, D, 32, kDrop>(a, s, err);
+    case 64: return bf16 ? run<true, D, 64, kDrop>(a, s, err) : run<false, D, 64, kDrop>(a, s, err);
+    case 128:
+      return bf16 ? run<true, D, 128, kDrop>(a, s, err) : run<false, D, 128, kDrop>(a, s, err);
     default: err = "kv_block must be 0, 32, 64 or 128"; return -2;
   }
+}
+
+template <int D>
+int launch_d(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
+  return a.dropout ? launch_dd<D, true>(bf16, a, s, err) : launch_dd<D, false>(bf16, a, s, err);
 }
 
 }  // namespace fwd

@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <string>
 
+#include "dropout.cuh"
+
 namespace ea {
 
 enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskBitmap = 2 };
@@ -26,6 +28,7 @@ struct FwdParams {
   int num_splits;
   float* o_part;
   float* lse_part;
+  DropoutArgs drop;  // read only by the dropout instantiations
 };
 
 // Everything a launcher needs; pointers are device pointers.
@@ -53,6 +56,8 @@ struct AttnArgs {
   int num_splits;   // forward: 1, or the number of key shards (partials go to o_part, lse_part)
   float* o_part;
   float* lse_part;
+  bool dropout;     // drop probabilities with the mask of dropout.cuh (p > 0)
+  DropoutArgs drop;
 };
 
 // Each launcher returns 0 or a negative ATTN_ERR_* code and fills `err` on failure.

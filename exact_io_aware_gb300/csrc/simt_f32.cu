@@ -13,6 +13,10 @@
 // Key split (gridDim.z > 1): CTA z walks only its share of the key blocks and writes its rows'
 // normalised partial (O_z, LSE_z) to the split buffers; a merge kernel combines the shares.
 //
+// Dropout (drop = true): the mask of dropout.cuh is drawn per (query, key) pair; kept
+// probabilities enter O and dV scaled by 1/(1-p), the normaliser keeps every probability, and
+// dS = P (keep ? dP/(1-p) : 0) - P D.
+//
 // Backward: two kernels, no atomics.  The dQ kernel walks key blocks past 32 query rows; the
 // dK/dV kernel walks query blocks past 32 key rows.  Both recompute s_ij and
 // p_ij = exp(s_ij - LSE_i) and use D_i = dO_i . O_i from the preprocessing kernel.
@@ -63,7 +67,8 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
                                                           const float* __restrict__ V,
                                                           float* __restrict__ O,
                                                           float* __restrict__ lse, float c,
-                                                          Mask mk, uint32_t* status) {
+                                                          Mask mk, uint32_t* status,
+                                                          DropoutArgs dr, bool drop) {
   extern __shared__ float sm[];
   float* sQ = sm;                       // [kRows][D]
   float* sK = sQ + kRows * D;           // [BN][D + 1]
@@ -130,6 +135,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
       for (int u = 0; u < NJ; ++u) {
         s[u] = expf(s[u] - mn);
         ps += s[u];
+        if (drop && !keep1(dr, static_cast<uint32_t>(i), static_cast<uint32_t>(key0 + u * 32 + lane),
+                           static_cast<uint32_t>(bh)))
+          s[u] = 0.0f;  // dropped: out of the value sum, still in the normaliser
       }
       l[q] = l[q] * scale + warp_sum(ps);
       m[q] = mn;
@@ -154,7 +162,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
     const int i = row_base + warp * kRowsPerWarp + q;
     if (i >= n) continue;
     const bool empty = !(l[q] > 0.0f);
-    const float inv = empty ? 0.0f : 1.0f / l[q];
+    const float inv = empty ? 0.0f : (drop ? dr.scale : 1.0f) / l[q];
 #pragma unroll
     for (int w = 0; w < NU; ++w) {
       const int col = w * 32 + lane;
@@ -172,7 +180,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarps * 32) dq_kernel(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ Dv,
-    float* __restrict__ dQ, float c, Mask mk) {
+    float* __restrict__ dQ, float c, Mask mk, DropoutArgs dr, bool drop) {
   constexpr int BN = 64;
   extern __shared__ float sm[];
   float* sQ = sm;                  // [kRows][D]
@@ -229,6 +237,9 @@ __global__ void __launch_bounds__(kWarps * 32) dq_kernel(
           pdot = fmaf(sG[r * D + col], sV[j * (D + 1) + col], pdot);
         }
         const float pij = mk.allowed(bh, i, key0 + j) ? expf(c * sdot - L[q]) : 0.0f;
+        if (drop)
+          pdot = keep1(dr, static_cast<uint32_t>(i), static_cast<uint32_t>(key0 + j),
+                       static_cast<uint32_t>(bh)) ? pdot * dr.scale : 0.0f;
         ds[u] = pij * (pdot - Dd[q]);
       }
 #pragma unroll
@@ -262,7 +273,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarps * 32) dkdv_kernel(
     const float* __restrict__ Q, const float* __restrict__ K, const float* __restrict__ V,
     const float* __restrict__ dO, const float* __restrict__ lse, const float* __restrict__ Dv,
-    float* __restrict__ dK, float* __restrict__ dV, float c, Mask mk) {
+    float* __restrict__ dK, float* __restrict__ dV, float c, Mask mk, DropoutArgs dr, bool drop) {
   constexpr int BM = 64;
   extern __shared__ float sm[];
   float* sK = sm;                  // [kRows][D]  this CTA's key rows
@@ -321,6 +332,12 @@ __global__ void __launch_bounds__(kWarps * 32) dkdv_kernel(
         const bool ok = sL[i] != -INFINITY && mk.allowed(bh, qb + i, j);
         const float pij = ok ? expf(c * sdot - sL[i]) : 0.0f;
         pp[u] = pij;
+        if (drop) {
+          const bool kept = keep1(dr, static_cast<uint32_t>(qb + i), static_cast<uint32_t>(j),
+                                  static_cast<uint32_t>(bh));
+          pp[u] = kept ? pij * dr.scale : 0.0f;
+          pdot = kept ? pdot * dr.scale : 0.0f;
+        }
         ds[u] = pij * (pdot - sD[i]);
       }
 #pragma unroll
@@ -381,7 +398,8 @@ int fwd_run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   k<<<grid, kWarps * 32, smem, s>>>(static_cast<const float*>(a.q), static_cast<const float*>(a.k),
                                     static_cast<const float*>(a.v),
                                     split ? a.o_part : static_cast<float*>(a.o_out),
-                                    split ? a.lse_part : a.lse, a.c, make_mask(a), a.status);
+                                    split ? a.lse_part : a.lse, a.c, make_mask(a), a.status,
+                                    a.drop, a.dropout);
   return 0;
 }
 
@@ -410,9 +428,10 @@ int bwd_d(const AttnArgs& a, const float* Dv, cudaStream_t s, std::string& err) 
   const float* v = static_cast<const float*>(a.v);
   const float* g = static_cast<const float*>(a.d_o);
   kq<<<grid, kWarps * 32, smem_q, s>>>(q, k, v, g, a.lse, Dv, static_cast<float*>(a.dq), a.c,
-                                       make_mask(a));
+                                       make_mask(a), a.drop, a.dropout);
   kk<<<grid, kWarps * 32, smem_k, s>>>(q, k, v, g, a.lse, Dv, static_cast<float*>(a.dk),
-                                       static_cast<float*>(a.dv), a.c, make_mask(a));
+                                       static_cast<float*>(a.dv), a.c, make_mask(a), a.drop,
+                                       a.dropout);
   return 0;
 }
 

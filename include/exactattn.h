@@ -96,6 +96,27 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c,
              void* o, float* lse, void* stream);
 
 /*
+ * Forward pass with dropout on the attention probabilities.  The pages' base procedure has no
+ * dropout and ask of any dropout extension that its reverse pass replay the realised mask
+ * ("Exact tiled attention and memory-aware differentiation", reverse procedure; closing
+ * remark).  Here the mask is a pure function of (seed, head, query row, key), so the forward
+ * and attn_bwd_dropout draw the same mask and no mask is stored:
+ *   words = Philox4x32-10(counter = (i, floor(j / 4), b * H + h, 0), key = (seed mod 2^32,
+ *           floor(seed / 2^32)))  (Salmon et al., "Parallel random numbers: as easy as 1, 2,
+ *           3", SC 2011); the pair (i, j) is kept iff words[j mod 4] >= floor(p_drop 2^32 + 1/2).
+ *   O_i = sum_j P_ij keep_ij V_j / (1 - p_drop), P = softmax as without dropout.
+ * LSE is that of the undropped scores (the statistic the backward needs).
+ *   p_drop  drop probability, 0 <= p_drop < 1 (0 gives exactly attn_fwd's result)
+ *   seed    64-bit generator key; the same (seed, p_drop) must be passed to attn_bwd_dropout
+ * Other arguments, outputs and errors as for attn_fwd.
+ */
+int attn_fwd_dropout(int dtype, int B, int H, int n, int d, float c,
+                     const void* q, const void* k, const void* v,
+                     int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                     int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed,
+                     void* o, float* lse, void* stream);
+
+/*
  * Key-split forward: the same O and LSE as attn_fwd, computed as num_splits partial results
  * over disjoint shares of the key blocks and combined by attn_merge's rule.  This is the
  * key-sharded reading of the merge of stable summaries in "Exact tiled attention and
@@ -165,6 +186,20 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c,
              int64_t mask_head_stride_words, int kv_block,
              void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
              void* stream);
+
+/*
+ * Backward pass of attn_fwd_dropout, replaying the same mask (same seed and p_drop).  With
+ * P~ = P * keep / (1 - p_drop): dV = P~^T dO;  D_i = dO_i . O_i (O the dropped output);
+ * dS_ij = P_ij (keep_ij (dO_i . V_j) / (1 - p_drop) - D_i);  dQ = c dS K,  dK = c dS^T Q.
+ * Other arguments, outputs, workspace and errors as for attn_bwd.
+ */
+int attn_bwd_dropout(int dtype, int B, int H, int n, int d, float c,
+                     const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* d_o,
+                     int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                     int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                     void* stream);
 
 /*
  * attn_bwd without a workspace argument, for callers that cannot allocate device memory at

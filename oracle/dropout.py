@@ -10,7 +10,7 @@ module restates:
 * Mask.  For head index bh (b·H + h), query row i and key j, the generator is
   Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
   1, 2, 3", SC 2011): counter (i, ⌊j/4⌋, bh, 0), key (seed mod 2^32, ⌊seed / 2^32⌋).  Word
-  j mod 4 of the output is compared with the integer threshold t = round(p·2^32): the
+  j mod 4 of the output is compared with the integer threshold t = ⌊p·2^32 + 1/2⌋: the
   pair (i, j) is kept iff word ≥ t.  Integer arithmetic end to end, so the mask is the same
   bit for bit wherever it is drawn.
 * Forward.  P_ij = exp(s_ij − LSE_i) as without dropout (LSE is not changed by dropout);
@@ -21,6 +21,8 @@ module restates:
   softmax, the mask held fixed.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -48,10 +50,10 @@ def philox4x32(ctr, key, rounds=10):
 
 
 def threshold(p):
-    """Integer drop threshold round(p·2^32) for a drop probability 0 <= p < 1."""
+    """Integer drop threshold ⌊p·2^32 + 1/2⌋ (halves round up) for 0 <= p < 1."""
     if not 0.0 <= p < 1.0:
         raise ValueError("drop probability must be in [0, 1)")
-    return int(round(p * 2.0 ** 32))
+    return int(math.floor(p * 2.0 ** 32 + 0.5))
 
 
 def keep_mask(seed, bh, rows, n, p):
