@@ -420,16 +420,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_spin(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
       if (!ok) break;
       // Dropout: keep bits of this key with the warp's query columns (bit k of word h <->
-      // query q0 + c_lo + 32 h + k), drawn while the scores are still being computed.
+      // query q0 + c_lo + 32 h + k), drawn while the scores are still being computed.  One
+      // generator call covers four consecutive keys of one query, and the four lanes of a key
+      // group (4 | key0 + 32 quad) share those keys: lane l draws the calls of queries
+      // 4g + (l & 3), g = 0..7, and the group swaps the 4-bit results with four shuffles.
       uint32_t kbits[kDrop ? kHalf / 32 : 1];
       if constexpr (kDrop) {
+        const uint32_t sub = static_cast<uint32_t>(lane & 3);
 #pragma unroll
         for (int h = 0; h < kHalf / 32; ++h) {
-          uint32_t w = 0;
+          uint32_t mine = 0;  // nibble g: keep bits of keys 4 (j / 4) .. +3 with query 4g + sub
 #pragma unroll 1
-          for (int k = 0; k < 32; ++k)
-            w |= (keep1(p.drop, static_cast<uint32_t>(q0 + c_lo + 32 * h + k),
-                        static_cast<uint32_t>(j), bh) ? 1u : 0u) << k;
+          for (int g = 0; g < 8; ++g)
+            mine |= keep4(p.drop, static_cast<uint32_t>(q0 + c_lo + 32 * h + 4 * g) + sub,
+                          static_cast<uint32_t>(j) >> 2, bh) << (4 * g);
+          uint32_t w = 0;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const uint32_t got = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) w |= ((got >> (4 * g + sub)) & 1u) << (4 * g + t);
+          }
           kbits[h] = w;
         }
       }

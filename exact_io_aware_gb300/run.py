@@ -42,6 +42,7 @@ def main(argv=None):
     ap.add_argument("--fwd-only", action="store_true")
     ap.add_argument("--splits", type=int, default=None,
                     help="forward through attn_fwd_split with this many key shares (0 = library choice)")
+    ap.add_argument("--dropout", type=float, default=0.0, help="drop probability (0 = none)")
     ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
 
@@ -83,14 +84,15 @@ def main(argv=None):
     for e in ev:
         e[0].record()
         if a.splits is None:
-            ea.attn_fwd(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse)
+            ea.attn_fwd(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse,
+                        dropout_p=a.dropout, seed=1234)
         else:
             ea.attn_fwd_split(q, k, v, c, mask=mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse,
                               num_splits=splits, workspace=fws)
         e[1].record()
         if not fwd_only:
             ea.attn_bwd(q, k, v, o, lse, do, c, mask=mask, mask_bits=bits, kv_block=kvb,
-                        workspace=ws)
+                        workspace=ws, dropout_p=a.dropout, seed=1234)
         e[2].record()
     torch.cuda.synchronize()
     status = ea.attn_device_status()
@@ -98,7 +100,7 @@ def main(argv=None):
     bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev[1:]])) if not fwd_only else None
     fl = 4.0 * B * H * n * n * d * kappa
     out = {"workload": name, "B": B, "H": H, "n": n, "d": d, "dtype": dtype, "mask": mask,
-           "kv_block": kvb, "splits": splits, "kappa": kappa, "fwd_ms": fwd_ms,
+           "kv_block": kvb, "splits": splits, "dropout": a.dropout, "kappa": kappa, "fwd_ms": fwd_ms,
            "fwd_tflops": fl / (fwd_ms / 1e3) / 1e12, "status": status}
     if bwd_ms is not None:
         out.update(bwd_ms=bwd_ms, bwd_tflops=2.5 * fl / (bwd_ms / 1e3) / 1e12)
