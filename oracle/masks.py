@@ -7,6 +7,9 @@ and query rows ``rows``, which keys are members of A_i.
 * causal — key j is allowed for query i iff j <= i (0-indexed, diagonal included): the
            "Night School: fused attention" page has each word score itself and every earlier
            word (section "The table of scores").
+* causal_rect — m query rows against n keys with the queries at the end of the sequence (the
+           decoding reading of a key/value cache: query i stands at position i + n - m), key j
+           allowed iff j <= i + n - m; m = n is the causal mask above.
 * bitmap — the caller-owned packed representation of the allowed sets named in "Exact tiled
            attention and memory-aware differentiation" (algorithm inputs: membership is read
            on demand from input storage).  Row-major ``[n][row_words]`` uint32 words; key j
@@ -31,6 +34,16 @@ def causal(n: int):
     def allowed(bh, rows):
         rows = np.asarray(rows).reshape(-1, 1)
         return keys[None, :] <= rows
+    return allowed
+
+
+def causal_rect(m: int, n: int):
+    keys = np.arange(n)
+    off = n - m
+
+    def allowed(bh, rows):
+        rows = np.asarray(rows).reshape(-1, 1)
+        return keys[None, :] <= rows + off
     return allowed
 
 

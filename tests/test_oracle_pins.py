@@ -396,6 +396,23 @@ def test_io_model_reproduces_printed_counts():
 
 # ---------------------------------------------------------------- mask storage
 
+def test_rectangular_causal_is_the_tail_of_square_attention():
+    # a key/value cache: the last m queries against all n keys give the last m rows of square
+    # causal attention over the n positions
+    rng = np.random.default_rng(61)
+    n, d = 50, 6
+    q, k, v = (rng.normal(size=(n, d)) for _ in range(3))
+    y, lse, _, _ = attention.forward_rows(q, k, v, 0.7, masks.causal(n)(0, np.arange(n)))
+    for m in (1, 3, 17, n):
+        mk = masks.causal_rect(m, n)
+        ym, lm, _, _ = attention.forward_rows(q[n - m:], k, v, 0.7, mk(0, np.arange(m)))
+        assert np.max(np.abs(ym - y[n - m:])) < 1e-13 and np.max(np.abs(lm - lse[n - m:])) < 1e-13
+    assert np.array_equal(masks.causal_rect(n, n)(0, np.arange(n)), masks.causal(n)(0, np.arange(n)))
+    assert masks.causal_rect(1, 9)(0, [0]).all()
+    a = masks.causal_rect(7, 4)(0, np.arange(7))  # more queries than keys: the first 3 see none
+    assert not a[:3].any() and a[3, :1].all() and not a[3, 1:].any() and a[6].all()
+
+
 def test_bitmap_membership_hand_built():
     n = 70
     words = np.zeros((2, 3), np.uint32)
