@@ -18,7 +18,7 @@ import os
 import torch
 
 __all__ = [
-    "attn_fwd_dropout", "attn_bwd_dropout",
+    "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_kv", "attn_fwd_kv_split_count",
     "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
@@ -84,6 +84,11 @@ def load():
     lib.attn_fwd_split_workspace_bytes.restype = sz
     lib.attn_merge.argtypes = [i32, i32, i64, i32, vp, vp, vp, vp, vp]
     lib.attn_merge.restype = i32
+    lib.attn_fwd_kv.argtypes = [i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
+                                i32, i32, vp, vp, vp, sz, vp]
+    lib.attn_fwd_kv.restype = i32
+    lib.attn_fwd_kv_split_count.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.attn_fwd_kv_split_count.restype = i32
     u64 = ctypes.c_uint64
     lib.attn_fwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
                                      i32, f32, u64, vp, vp, vp]
@@ -191,6 +196,41 @@ def attn_fwd_split(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_wor
                                  _ptr(o), _ptr(lse), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_fwd_kv_split_count(dtype, B, H, n_q, n_kv, d, kv_block=0) -> int:
+    """Key shares attn_fwd_kv uses with num_splits=0 on the current device."""
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return int(load().attn_fwd_kv_split_count(code, B, H, n_q, n_kv, d, int(kv_block)))
+
+
+def attn_fwd_kv(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=0, kv_block=0,
+                num_splits=0, o=None, lse=None, workspace=None, stream=None):
+    """Forward of q [B,H,n_q,d] against a key/value cache k, v [B,H,n_kv,d] (queries at the end
+    of the sequence under the causal mask); returns (o [B,H,n_q,d], lse [B,H,n_q])."""
+    if q.dim() != 4 or k.shape != v.shape or k.dim() != 4:
+        raise ValueError("q must be [B,H,n_q,d] and k, v [B,H,n_kv,d]")
+    B, H, n_q, d = q.shape
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("q, k, v must agree on B, H and d")
+    n_kv = k.shape[2]
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != q.dtype or t.dtype not in DTYPE_CODE:
+            raise ValueError("q, k, v must be contiguous CUDA tensors of one supported dtype")
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    splits = int(num_splits) or attn_fwd_kv_split_count(q.dtype, B, H, n_q, n_kv, d, kv_block)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q.device)
+    need = attn_fwd_split_workspace_bytes(q.dtype, B, H, n_q, d, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(load().attn_fwd_kv(DTYPE_CODE[q.dtype], B, H, n_q, n_kv, d, float(c), _ptr(q), _ptr(k),
+                              _ptr(v), kind, _ptr(bits), row_words, hs, int(kv_block), splits,
+                              _ptr(o), _ptr(lse), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
     return o, lse
 
 

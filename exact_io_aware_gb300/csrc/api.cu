@@ -66,25 +66,52 @@ int sm_count() {
   return cached[dev];
 }
 
-// Library choice of the key split: enough shares that the forward grid covers every
-// multiprocessor once, at most one share per key block and at most kMaxSplits.
-int auto_splits(int dtype, int B, int H, int n, int kv_block) {
+// Library choice of the key split (at most one share per key block and at most kMaxSplits).
+// With several query tiles per head: no split once the tiles fill the multiprocessors (a split
+// adds float32 partials of every row), else enough shares for one full wave.  With a single
+// query tile per head (a key/value cache read by a few queries, where the keys are the work):
+// the smallest share count whose CTAs cover every multiprocessor and fill the last wave at
+// least 90 %, failing that the count with the fullest waves.
+int auto_splits(int dtype, int B, int H, int nq, int nk, int kv_block) {
   const int rows_per_cta = dtype == ATTN_F32 ? 32 : 256;
   const int bn = kv_block ? kv_block : (dtype == ATTN_F32 ? 64 : 128);
-  const int64_t ctas = static_cast<int64_t>((n + rows_per_cta - 1) / rows_per_cta) * B * H;
+  const int64_t ctas = static_cast<int64_t>((nq + rows_per_cta - 1) / rows_per_cta) * B * H;
   const int sms = sm_count();
-  int splits = sms > 0 ? static_cast<int>((sms + ctas - 1) / ctas) : 1;
-  splits = std::min(splits, (n + bn - 1) / bn);
-  return std::max(1, std::min(splits, kMaxSplits));
+  const int max_s = std::min(kMaxSplits, (nk + bn - 1) / bn);
+  if (sms <= 0 || max_s <= 1) return 1;
+  if (nq > rows_per_cta) {
+    if (ctas >= sms) return 1;
+    return static_cast<int>(std::min<int64_t>(max_s, (sms + ctas - 1) / ctas));
+  }
+  int best = 1;
+  double best_fill = 0.0;
+  for (int sp = 1; sp <= max_s; ++sp) {
+    const int64_t total = ctas * sp;
+    const int64_t waves = (total + sms - 1) / sms;
+    const double fill = static_cast<double>(total) / static_cast<double>(waves * sms);
+    if (total >= sms && fill >= 0.9) return sp;
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = sp;
+    }
+  }
+  return best;
 }
 
 size_t split_part_bytes(int B, int H, int n, int d, int splits) {
   return round256(static_cast<size_t>(splits) * B * H * n * d * sizeof(float));
 }
 
+size_t split_ws_bytes(int B, int H, int n, int d, int splits) {
+  return split_part_bytes(B, H, n, d, splits) +
+         round256(static_cast<size_t>(splits) * B * H * n * sizeof(float));
+}
+
+// n: query rows; nk: keys (the bitmap's words cover the keys).
 int check_common(int dtype, int B, int H, int n, int d, const void* q, const void* k,
                  const void* v, int mask_kind, const uint32_t* bits, int64_t row_words,
-                 int64_t head_stride, int kv_block) {
+                 int64_t head_stride, int kv_block, int nk = -1) {
+  if (nk < 0) nk = n;
   if (dtype < ATTN_F32 || dtype > ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype");
   if (B < 1 || H < 1 || n < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and n must be positive");
   if (d != 16 && d != 32 && d != 64 && d != 128)
@@ -102,7 +129,8 @@ int check_common(int dtype, int B, int H, int n, int d, const void* q, const voi
     if (!bits) return fail(ATTN_ERR_INVALID_ARG, "bitmap mask without mask_bits");
     if ((reinterpret_cast<uintptr_t>(bits) & 3u) != 0)
       return fail(ATTN_ERR_ALIGNMENT, "mask_bits must be 4-byte aligned");
-    if (row_words < (n + 31) / 32) return fail(ATTN_ERR_INVALID_ARG, "mask_row_words < ceil(n/32)");
+    if (row_words < (nk + 31) / 32)
+      return fail(ATTN_ERR_INVALID_ARG, "mask_row_words < ceil(keys/32)");
     if (head_stride < 0) return fail(ATTN_ERR_INVALID_ARG, "negative mask_head_stride_words");
   }
   return ATTN_OK;
@@ -126,6 +154,7 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.mask_head_stride_words = head_stride;
   a.kv_block = kv_block;
   a.num_splits = 1;
+  a.nk = n;
   return a;
 }
 
@@ -162,28 +191,50 @@ int set_dropout(float p_drop, uint64_t seed, ea::AttnArgs& a) {
   return ATTN_OK;
 }
 
-int fwd_impl(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
-             const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
-             int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed, void* o,
-             float* lse, void* stream) {
-  if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
-                            mask_head_stride_words, kv_block))
+// Every forward entry point: nq query rows against nk keys (nk = nq for square attention),
+// optional dropout, and a key split of `splits` shares (1 = one pass straight into o, lse).
+int fwd_general(int dtype, int B, int H, int nq, int nk, int d, float c, const void* q,
+                const void* k, const void* v, int mask_kind, const uint32_t* mask_bits,
+                int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
+                float p_drop, uint64_t seed, int splits, void* o, float* lse, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (nk < 1) return fail(ATTN_ERR_INVALID_ARG, "the key length must be positive");
+  if (int rc = check_common(dtype, B, H, nq, d, q, k, v, mask_kind, mask_bits, mask_row_words,
+                            mask_head_stride_words, kv_block, nk))
     return rc;
   if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
   if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
-  ea::AttnArgs a = make_args(B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+  ea::AttnArgs a = make_args(B, H, nq, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                              mask_head_stride_words, kv_block);
+  a.nk = nk;
   a.o_out = o;
   a.lse = lse;
   if (int rc = set_dropout(p_drop, seed, a)) return rc;
+  if (splits > 1) {
+    const size_t need = split_ws_bytes(B, H, nq, d, splits);
+    if (!workspace || workspace_bytes < need)
+      return fail(ATTN_ERR_WORKSPACE,
+                  "workspace missing or smaller than attn_fwd_split_workspace_bytes");
+    if (!aligned16(workspace))
+      return fail(ATTN_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+    a.num_splits = splits;
+    a.o_part = static_cast<float*>(workspace);
+    a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          split_part_bytes(B, H, nq, d, splits));
+  }
   if (int rc = status_ptr(&a.status)) return rc;
   std::string err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc = dtype == ATTN_F32 ? ea::launch_fwd_f32(a, s, err)
                              : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
   if (rc) return fail(rc, err);
+  if (splits > 1) {
+    rc = ea::launch_merge(dtype, splits, static_cast<int64_t>(B) * H * nq, d, a.o_part,
+                          a.lse_part, o, lse, a.status, s, err);
+    if (rc) return fail(rc, err);
+  }
   return ATTN_OK;
 }
 
@@ -194,29 +245,34 @@ extern "C" {
 int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
              const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
              int64_t mask_head_stride_words, int kv_block, void* o, float* lse, void* stream) {
-  return fwd_impl(dtype, B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
-                  mask_head_stride_words, kv_block, 0.0f, 0, o, lse, stream);
+  return fwd_general(dtype, B, H, n, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                     mask_head_stride_words, kv_block, 0.0f, 0, 1, o, lse, nullptr, 0, stream);
 }
 
 int attn_fwd_dropout(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
                      const void* v, int mask_kind, const uint32_t* mask_bits,
                      int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                      float p_drop, uint64_t seed, void* o, float* lse, void* stream) {
-  return fwd_impl(dtype, B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
-                  mask_head_stride_words, kv_block, p_drop, seed, o, lse, stream);
+  return fwd_general(dtype, B, H, n, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                     mask_head_stride_words, kv_block, p_drop, seed, 1, o, lse, nullptr, 0,
+                     stream);
 }
 
 int attn_fwd_split_count(int dtype, int B, int H, int n, int d, int kv_block) {
   if (B < 1 || H < 1 || n < 1 || d < 1) return 0;
-  return auto_splits(dtype, B, H, n, kv_block);
+  return auto_splits(dtype, B, H, n, n, kv_block);
+}
+
+int attn_fwd_kv_split_count(int dtype, int B, int H, int n_q, int n_kv, int d, int kv_block) {
+  if (B < 1 || H < 1 || n_q < 1 || n_kv < 1 || d < 1) return 0;
+  return auto_splits(dtype, B, H, n_q, n_kv, kv_block);
 }
 
 size_t attn_fwd_split_workspace_bytes(int dtype, int B, int H, int n, int d, int num_splits) {
   (void)dtype;
   if (B < 1 || H < 1 || n < 1 || d < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
   if (num_splits == 1) return 0;
-  return split_part_bytes(B, H, n, d, num_splits) +
-         round256(static_cast<size_t>(num_splits) * B * H * n * sizeof(float));
+  return split_ws_bytes(B, H, n, d, num_splits);
 }
 
 int attn_fwd_split(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
@@ -225,38 +281,26 @@ int attn_fwd_split(int dtype, int B, int H, int n, int d, float c, const void* q
                    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (num_splits < 0 || num_splits > kMaxSplits)
     return fail(ATTN_ERR_INVALID_ARG, "num_splits must be 0 (library choice) or 1..32");
-  if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
-                            mask_head_stride_words, kv_block))
-    return rc;
-  const int splits = num_splits ? num_splits : auto_splits(dtype, B, H, n, kv_block);
-  if (splits == 1)
-    return attn_fwd(dtype, B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
-                    mask_head_stride_words, kv_block, o, lse, stream);
-  if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
-  if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
-    return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
-  const size_t need = attn_fwd_split_workspace_bytes(dtype, B, H, n, d, splits);
-  if (!workspace || workspace_bytes < need)
-    return fail(ATTN_ERR_WORKSPACE,
-                "workspace missing or smaller than attn_fwd_split_workspace_bytes");
-  if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
-  ea::AttnArgs a = make_args(B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
-                             mask_head_stride_words, kv_block);
-  a.num_splits = splits;
-  a.o_part = static_cast<float*>(workspace);
-  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        split_part_bytes(B, H, n, d, splits));
-  if (int rc = status_ptr(&a.status)) return rc;
-  std::string err;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int rc = dtype == ATTN_F32 ? ea::launch_fwd_f32(a, s, err)
-                             : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
-  if (rc) return fail(rc, err);
-  rc = ea::launch_merge(dtype, splits, static_cast<int64_t>(B) * H * n, d, a.o_part, a.lse_part,
-                        o, lse, a.status, s, err);
-  if (rc) return fail(rc, err);
-  return ATTN_OK;
+  if (B < 1 || H < 1 || n < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and n must be positive");
+  const int splits = num_splits ? num_splits : auto_splits(dtype, B, H, n, n, kv_block);
+  return fwd_general(dtype, B, H, n, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+                     mask_head_stride_words, kv_block, 0.0f, 0, splits, o, lse, workspace,
+                     workspace_bytes, stream);
+}
+
+int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c, const void* q,
+                const void* k, const void* v, int mask_kind, const uint32_t* mask_bits,
+                int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
+                int num_splits, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                void* stream) {
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(ATTN_ERR_INVALID_ARG, "num_splits must be 0 (library choice) or 1..32");
+  if (B < 1 || H < 1 || n_q < 1 || n_kv < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, n_q and n_kv must be positive");
+  const int splits = num_splits ? num_splits : auto_splits(dtype, B, H, n_q, n_kv, kv_block);
+  return fwd_general(dtype, B, H, n_q, n_kv, d, c, q, k, v, mask_kind, mask_bits,
+                     mask_row_words, mask_head_stride_words, kv_block, 0.0f, 0, splits, o, lse,
+                     workspace, workspace_bytes, stream);
 }
 
 int attn_merge(int dtype, int num_parts, int64_t rows, int d, const float* o_parts,

@@ -22,6 +22,10 @@
 // The issuers have the lowest warp slots, which the warp schedulers favour over the
 // softmax warps they share a sub-partition with.
 //
+// Query and key lengths may differ (a key/value cache): p.n query rows against p.nk keys, and
+// under the causal mask query i sees keys j <= i + p.off (off = nk - n: the queries are the
+// last rows of the sequence).  With n = nk this is ordinary causal attention.
+//
 // Key split (gridDim.z > 1): the pair's key blocks are cut into gridDim.z contiguous shares and
 // CTA z walks share z only.  It writes its rows' summary of that share in normalised form,
 // O_z = z/l (float32) and LSE_z = m + ln l (-inf for a row with no allowed key in the share),
@@ -117,17 +121,17 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 // query tiles (rows r0 .. r0 + 127 of the pair) whether it skips the block, takes it whole or
 // needs the mask pass (causal diagonal or the ragged key tail).  Same encoding as the bitmap
 // table: j | cls0 << 16 | cls1 << 18.
-__device__ __forceinline__ uint32_t dense_step(int j, int BN, int nblk, int n, int pair_row0,
-                                               bool causal) {
+__device__ __forceinline__ uint32_t dense_step(int j, int BN, int nblk, int n, int nk, int off,
+                                               int pair_row0, bool causal) {
   uint32_t w = static_cast<uint32_t>(j);
-  const bool tail_blk = (n % BN) != 0 && j == nblk - 1;
+  const bool tail_blk = (nk % BN) != 0 && j == nblk - 1;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = pair_row0 + t * kRowsPerTile;
     if (r0 >= n) continue;
     const int last_row = min(r0 + kRowsPerTile, n) - 1;
-    const bool any = !causal || j * BN <= last_row;
-    const bool all = !causal || (j + 1) * BN - 1 <= r0;
+    const bool any = !causal || j * BN <= last_row + off;
+    const bool all = !causal || (j + 1) * BN - 1 <= r0 + off;
     const uint32_t cls = any ? ((all && !tail_blk) ? kFull : kPartial) : kSkip;
     w |= cls << (16 + 2 * t);
   }
@@ -156,11 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int n = p.n;
+  const int n = p.n;    // query rows
+  const int nk = p.nk;  // keys
+  const int off = p.off;
   const int bh = blockIdx.y;
   const int pair = (gridDim.x - 1 - blockIdx.x);  // heaviest (causal) query tiles first
   const int pair_row0 = pair * 2 * kRowsPerTile;  // tile t starts at pair_row0 + 128 t
-  const int nblk = (n + BN - 1) / BN;
+  const int nblk = (nk + BN - 1) / BN;
   const int split = blockIdx.z;
   const int nsplit = gridDim.z;
   const bool partial_out = p.o_part != nullptr;
@@ -184,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool use_table = p.mask_kind == kMaskBitmap;
   const bool causal = p.mask_kind == kMaskCausal;
   const int pair_last = min(pair_row0 + 2 * kRowsPerTile, n) - 1;  // last row of the pair
-  const int reach = use_table ? nblk : (causal ? pair_last / BN + 1 : nblk);  // blocks walked
+  const int last_key = pair_last + off;  // causal: the last key the pair's rows see
+  const int reach = use_table ? nblk : (causal ? (last_key < 0 ? 0 : last_key / BN + 1) : nblk);
   const int share = (reach + nsplit - 1) / nsplit;
   const int j_lo = min(split * share, reach);
   const int j_hi = min(j_lo + share, reach);
@@ -204,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < BN / 32; ++q) {
             const int key0 = j * BN + q * 32;
-            if (key0 < n) {
+            if (key0 < nk) {
               uint32_t w = __ldg(rowbits + key0 / 32);
-              const int nk = n - key0;
-              const uint32_t live = nk >= 32 ? 0xFFFFFFFFu : ((1u << nk) - 1u);
+              const int left = nk - key0;
+              const uint32_t live = left >= 32 ? 0xFFFFFFFFu : ((1u << left) - 1u);
               w &= live;
               any |= w != 0;
               all &= w == live;
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     if (tid == 0) {
-      const bool tail = (n % BN) != 0;
+      const bool tail = (nk % BN) != 0;
       int ns = 0;
       for (int j = j_lo; j < j_hi; ++j) {
         const uint32_t b = steps[j];
@@ -246,7 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       const int r0 = pair_row0 + t * kRowsPerTile;
       if (r0 >= n || j_lo >= j_hi) continue;
-      const int last_blk = causal ? (min(r0 + kRowsPerTile, n) - 1) / BN : nblk - 1;
+      const int tile_last_key = min(r0 + kRowsPerTile, n) - 1 + off;
+      if (causal && tile_last_key < 0) continue;  // no row of the tile sees a key
+      const int last_blk = causal ? tile_last_key / BN : nblk - 1;
       if (j_lo <= last_blk) act |= 1u << t;
     }
     bars.act = act;
@@ -267,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t act = bars.act;
   // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*D
   auto step_at = [&](int i) -> uint32_t {
-    return use_table ? steps[i] : dense_step(j_lo + i, BN, nblk, n, pair_row0, causal);
+    return use_table ? steps[i] : dense_step(j_lo + i, BN, nblk, n, nk, off, pair_row0, causal);
   };
 
   if (warp == kProducerWarp) {
@@ -454,12 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kq = key0 + q * 32;
           uint32_t w;
           if (p.mask_kind == kMaskBitmap) {
-            w = (row < n && kq < n) ? __ldg(rowbits + kq / 32) : 0u;
-            const int nk = n - kq;
-            if (nk < 32) w &= nk > 0 ? (1u << nk) - 1u : 0u;
+            w = (row < n && kq < nk) ? __ldg(rowbits + kq / 32) : 0u;
+            const int left = nk - kq;
+            if (left < 32) w &= left > 0 ? (1u << left) - 1u : 0u;
           } else {
-            // allowed keys kq .. lim: lim = min(row, n - 1) (causal) or n - 1 (key tail)
-            const int lim = p.mask_kind == kMaskCausal ? min(row, n - 1) : n - 1;
+            // allowed keys kq .. lim: lim = min(row + off, nk - 1) (causal) or nk - 1 (key tail)
+            const int lim = p.mask_kind == kMaskCausal ? min(row + off, nk - 1) : nk - 1;
             const int cnt = min(max(lim - kq + 1, 0), 32);
             w = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
           }

@@ -12,7 +12,8 @@ namespace fwd {
 template <bool kBf16, int D, int BN, bool kDrop>
 int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   using Cfg = Config<D, BN>;
-  const size_t smem = Cfg::smem_bytes(a.n, a.mask_kind);
+  const int nk = a.nk > 0 ? a.nk : a.n;
+  const size_t smem = Cfg::smem_bytes(nk, a.mask_kind);
   if (smem > static_cast<size_t>(kMaxDynSmem)) {
     err = "n too large for the bitmap step table of the forward at this key block (use a "
           "smaller kv_block)";
@@ -22,8 +23,8 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   CUtensorMap tq, tk, tv, to;
   constexpr uint32_t bc = RowLayout<D>::kBoxCols;
   if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, kRowsPerTile, bc) ||
-      !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, BN, bc) ||
-      !encode_tile_map(&tv, a.v, kBf16, heads, a.n, D, BN, bc) ||
+      !encode_tile_map(&tk, a.k, kBf16, heads, nk, D, BN, bc) ||
+      !encode_tile_map(&tv, a.v, kBf16, heads, nk, D, BN, bc) ||
       !encode_tile_map(&to, a.o_out, kBf16, heads, a.n, D, kRowsPerTile, bc)) {
     err = "cuTensorMapEncodeTiled rejected a forward tensor map";
     return -5;
@@ -38,7 +39,7 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   const int nsplit = a.num_splits > 1 ? a.num_splits : 1;
   FwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
               a.lse, a.status, nsplit, nsplit > 1 ? a.o_part : nullptr,
-              nsplit > 1 ? a.lse_part : nullptr, a.drop};
+              nsplit > 1 ? a.lse_part : nullptr, a.drop, nk, nk - a.n};
   dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads),
             static_cast<unsigned>(nsplit));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);

@@ -14,7 +14,7 @@ enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskBitmap = 2 };
 
 // Scalar arguments of the forward kernels (tensor maps travel separately).
 struct FwdParams {
-  int n;
+  int n;    // query rows
   float c;
   int mask_kind;
   const uint32_t* mask_bits;
@@ -29,11 +29,14 @@ struct FwdParams {
   float* o_part;
   float* lse_part;
   DropoutArgs drop;  // read only by the dropout instantiations
+  int nk;            // keys (n for square attention)
+  int off;           // causal offset nk - n: query i sees keys j <= i + off
 };
 
 // Everything a launcher needs; pointers are device pointers.
 struct AttnArgs {
   int B, H, n, d;
+  int nk;  // keys; the forward allows nk != n (queries at the end of the key sequence)
   float c;
   const void* q;
   const void* k;

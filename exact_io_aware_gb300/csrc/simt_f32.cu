@@ -34,13 +34,15 @@ constexpr int kRows = kWarps * kRowsPerWarp;  // 32 rows per CTA
 
 struct Mask {
   int kind;
-  int n;
+  int n;  // query rows
   const uint32_t* bits;
   int64_t row_words;
   int64_t head_stride;
+  int nk;   // keys
+  int off;  // causal: query i sees keys j <= i + off
   __device__ __forceinline__ bool allowed(int bh, int i, int j) const {
-    if (j >= n || i >= n) return false;
-    if (kind == kMaskCausal) return j <= i;
+    if (j >= nk || i >= n) return false;
+    if (kind == kMaskCausal) return j <= i + off;
     if (kind == kMaskBitmap) {
       const uint32_t w = __ldg(bits + bh * head_stride + static_cast<int64_t>(i) * row_words + j / 32);
       return (w >> (j % 32)) & 1u;
@@ -75,10 +77,12 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
   float* sV = sK + BN * (D + 1);        // [BN][D]
   constexpr int NU = (D + 31) / 32;     // output columns per lane
   constexpr int NJ = BN / 32;           // keys per lane per block
-  const int n = mk.n;
+  const int n = mk.n;    // query rows
+  const int nk = mk.nk;  // keys
   const int bh = blockIdx.y;
   const int row_base = blockIdx.x * kRows;
-  const size_t head = static_cast<size_t>(bh) * n * D;
+  const size_t head = static_cast<size_t>(bh) * n * D;      // Q rows of this head
+  const size_t kv_head = static_cast<size_t>(bh) * nk * D;  // K, V rows of this head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool partial_out = gridDim.z > 1;  // O, lse point at the split buffers
   const size_t out_head = (static_cast<size_t>(blockIdx.z) * gridDim.y + bh) * n;
@@ -96,7 +100,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
     for (int u = 0; u < NU; ++u) z[q][u] = 0.0f;
   }
   const int last_row = min(row_base + kRows, n) - 1;
-  const int key_end = mk.kind == kMaskCausal ? last_row + 1 : n;
+  const int key_end = mk.kind == kMaskCausal ? max(0, min(nk, last_row + mk.off + 1)) : nk;
   const int reach = (key_end + BN - 1) / BN;  // key blocks the rows reach
   const int share = (reach + gridDim.z - 1) / gridDim.z;
   const int kb_lo = min(static_cast<int>(blockIdx.z) * share, reach);
@@ -105,9 +109,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_kernel(const float* __restric
     __syncthreads();
     for (int e = threadIdx.x; e < BN * D; e += blockDim.x) {
       const int j = e / D, col = e % D;
-      const bool in = key0 + j < n;
-      sK[j * (D + 1) + col] = in ? K[head + static_cast<size_t>(key0 + j) * D + col] : 0.0f;
-      sV[j * D + col] = in ? V[head + static_cast<size_t>(key0 + j) * D + col] : 0.0f;
+      const bool in = key0 + j < nk;
+      sK[j * (D + 1) + col] = in ? K[kv_head + static_cast<size_t>(key0 + j) * D + col] : 0.0f;
+      sV[j * D + col] = in ? V[kv_head + static_cast<size_t>(key0 + j) * D + col] : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -385,7 +389,9 @@ int set_smem(Kern k, size_t bytes, std::string& err) {
 }
 
 inline Mask make_mask(const AttnArgs& a) {
-  return Mask{a.mask_kind, a.n, a.mask_bits, a.mask_row_words, a.mask_head_stride_words};
+  const int nk = a.nk > 0 ? a.nk : a.n;
+  return Mask{a.mask_kind, a.n, a.mask_bits, a.mask_row_words, a.mask_head_stride_words, nk,
+              nk - a.n};
 }
 
 template <int D, int BN>

@@ -43,6 +43,8 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=None,
                     help="forward through attn_fwd_split with this many key shares (0 = library choice)")
     ap.add_argument("--dropout", type=float, default=0.0, help="drop probability (0 = none)")
+    ap.add_argument("--n-kv", type=int, default=0,
+                    help="keys of a key/value cache (forward of --n query rows through attn_fwd_kv)")
     ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
 
@@ -66,6 +68,8 @@ def main(argv=None):
             bits = torch.from_numpy(pack_bitmap(allowed).view(np.int32)).cuda()
     dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[dtype]
     ea.load()
+    if a.n_kv:
+        return _run_kv(a, B, H, n, a.n_kv, d, dt, mask, c, kvb)
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     shape = (B, H, n, d)
@@ -108,6 +112,44 @@ def main(argv=None):
         print(json.dumps(out))
     else:
         print(" ".join(f"{k}={v:.4g}" if isinstance(v, float) else f"{k}={v}" for k, v in out.items()))
+    return 0 if status == ea.ATTN_OK else 1
+
+
+def _run_kv(a, B, H, nq, nk, d, dt, mask, c, kvb):
+    """Forward of nq query rows against an nk-key cache; time and K/V bytes streamed."""
+    import numpy as np
+    import torch
+
+    import exact_io_aware_gb300 as ea
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    q = torch.randn((B, H, nq, d), device="cuda", generator=g).to(dt)
+    k = torch.randn((B, H, nk, d), device="cuda", generator=g).to(dt)
+    v = torch.randn((B, H, nk, d), device="cuda", generator=g).to(dt)
+    splits = a.splits if a.splits else ea.attn_fwd_kv_split_count(dt, B, H, nq, nk, d, kvb)
+    ws = torch.empty(max(16, ea.attn_fwd_split_workspace_bytes(dt, B, H, nq, d, splits)),
+                     dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, nq), device="cuda", dtype=torch.float32)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.iters + 1)]
+    for e in ev:
+        e[0].record()
+        ea.attn_fwd_kv(q, k, v, c, mask=mask, kv_block=kvb, num_splits=splits, o=o, lse=lse,
+                       workspace=ws)
+        e[1].record()
+    torch.cuda.synchronize()
+    status = ea.attn_device_status()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
+    if mask == "causal":  # query i sees keys <= i + nk - nq
+        pairs = sum(max(0, min(nk, i + nk - nq + 1)) for i in range(nq))
+    else:
+        pairs = nq * nk
+    kv_bytes = 2 * B * H * nk * d * q.element_size()
+    out = {"workload": "kv_cache", "B": B, "H": H, "n_q": nq, "n_kv": nk, "d": d,
+           "dtype": str(dt).split(".")[-1], "mask": mask, "splits": splits, "fwd_ms": ms,
+           "fwd_tflops": 4.0 * B * H * pairs * d / (ms / 1e3) / 1e12,
+           "kv_gbs": kv_bytes / (ms / 1e3) / 1e9, "kv_bytes": kv_bytes, "status": status}
+    print(json.dumps(out) if a.json else " ".join(f"{k}={v}" for k, v in out.items()))
     return 0 if status == ea.ATTN_OK else 1
 
 

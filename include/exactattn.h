@@ -138,6 +138,29 @@ int attn_fwd_split(int dtype, int B, int H, int n, int d, float c,
                    int64_t mask_head_stride_words, int kv_block, int num_splits,
                    void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Forward pass of n_q query rows against n_kv keys: attention over a key/value cache (for
+ * instance decoding, n_q small and n_kv long).  q and o are [B][H][n_q][d], k and v
+ * [B][H][n_kv][d], lse [B][H][n_q].  The queries are the last n_q positions of the sequence:
+ * under ATTN_MASK_CAUSAL query i sees keys j <= i + n_kv - n_q (n_q = n_kv is attn_fwd's causal
+ * mask; with n_q > n_kv the first n_q - n_kv rows see no key and are empty rows).  A bitmap has
+ * n_q rows of mask_row_words >= ceil(n_kv / 32) words.  The keys are cut into num_splits shares
+ * as in attn_fwd_split (0 = attn_fwd_kv_split_count), which is what fills the GPU when n_q is
+ * small; workspace as for attn_fwd_split with n = n_q (attn_fwd_split_workspace_bytes).
+ * The pages' tiled forward and its merge of stable summaries of disjoint key sets define the
+ * result for any query and key counts ("Exact tiled attention and memory-aware
+ * differentiation": inputs n queries, keys and values of any length).  Forward only: the
+ * backward entry points require n_q = n_kv.  Other arguments and errors as for attn_fwd_split.
+ */
+int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c,
+                const void* q, const void* k, const void* v,
+                int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                int64_t mask_head_stride_words, int kv_block, int num_splits,
+                void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The number of key shares attn_fwd_kv uses when num_splits = 0 on the current device. */
+int attn_fwd_kv_split_count(int dtype, int B, int H, int n_q, int n_kv, int d, int kv_block);
+
 /* The number of key shares attn_fwd_split uses when num_splits = 0 on the current device:
  * enough that the forward grid covers every multiprocessor, at most one per key block and
  * at most 32.  0 for non-positive sizes. */
