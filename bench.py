@@ -300,7 +300,7 @@ def run_ours(args):
     # on their own streams while step i computes (the link carries both directions at once).
     h_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
     h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
-    e2e_steps = max(2, min(args.steps, 10))
+    e2e_steps = max(2, min(args.steps, 30))
     sets = []
     for _ in range(2):
         d_in = [torch.empty_like(t) for t in (q, k, v, do)]
