@@ -9,6 +9,7 @@ the pages on exact IO-aware attention:
 * ``masks``      — allowed-key sets: none, causal, and the packed bitmap the library reads.
 * ``io_model``   — a global-memory byte counter for the unfused and fused kernels of the
                    "Night School: fused attention" lab.
+* ``fp8``        — E4M3 rounding and the FP8 forward's exact reference with its error bound.
 * ``dropout``    — the dropout extension with a replayed realised mask (Philox4x32-10 mask,
                    forward and reverse pass with the mask held fixed).
 
@@ -17,4 +18,4 @@ this package.  The GPU library never does, and this package imports nothing from
 Every function here is pinned by ``-m "not gpu"`` tests against worked examples, closed
 forms, invariants or brute force; none is marked "parity unpinned".
 """
-from . import attention, dropout, io_model, masks, tiled  # noqa: F401
+from . import attention, dropout, fp8, io_model, masks, tiled  # noqa: F401
