@@ -19,6 +19,7 @@ import torch
 
 __all__ = [
     "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_kv", "attn_fwd_kv_split_count",
+    "attn_fwd_fp8",
     "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
@@ -89,6 +90,9 @@ def load():
     lib.attn_fwd_kv.restype = i32
     lib.attn_fwd_kv_split_count.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.attn_fwd_kv_split_count.restype = i32
+    lib.attn_fwd_fp8.argtypes = [i32, i32, i32, i32, f32, vp, vp, vp, f32, f32, f32, i32, vp, i64,
+                                 i64, vp, vp, vp]
+    lib.attn_fwd_fp8.restype = i32
     u64 = ctypes.c_uint64
     lib.attn_fwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
                                      i32, f32, u64, vp, vp, vp]
@@ -231,6 +235,35 @@ def attn_fwd_kv(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=
                               _ptr(v), kind, _ptr(bits), row_words, hs, int(kv_block), splits,
                               _ptr(o), _ptr(lse), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+    return o, lse
+
+
+def _fp8_bytes(t, name):
+    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise ValueError(f"{name} must hold E4M3 values (torch.float8_e4m3fn or uint8)")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+def attn_fwd_fp8(q8, k8, vt8, c, q_scale, k_scale, v_scale, mask="none", mask_bits=None,
+                 mask_head_stride_words=0, o=None, lse=None, stream=None):
+    """FP8 forward: q8, k8 E4M3 [B,H,n,d], vt8 E4M3 [B,H,d,n] (V transposed), one scale per
+    tensor; returns (o bfloat16 [B,H,n,d], lse float32 [B,H,n])."""
+    q8, k8, vt8 = (_fp8_bytes(t, nm) for t, nm in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")))
+    if q8.dim() != 4 or k8.shape != q8.shape:
+        raise ValueError("q8 and k8 must be [B,H,n,d]")
+    B, H, n, d = q8.shape
+    if tuple(vt8.shape) != (B, H, d, n):
+        raise ValueError("vt8 must be [B,H,d,n] (V transposed)")
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    if o is None:
+        o = torch.empty((B, H, n, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, n), dtype=torch.float32, device=q8.device)
+    _check(load().attn_fwd_fp8(B, H, n, d, float(c), _ptr(q8), _ptr(k8), _ptr(vt8),
+                               float(q_scale), float(k_scale), float(v_scale), kind, _ptr(bits),
+                               row_words, hs, _ptr(o), _ptr(lse), _stream_ptr(stream)))
     return o, lse
 
 

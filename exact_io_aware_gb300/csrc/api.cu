@@ -303,6 +303,34 @@ int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c, cons
                      workspace, workspace_bytes, stream);
 }
 
+int attn_fwd_fp8(int B, int H, int n, int d, float c, const void* q8, const void* k8,
+                 const void* vt8, float q_scale, float k_scale, float v_scale, int mask_kind,
+                 const uint32_t* mask_bits, int64_t mask_row_words,
+                 int64_t mask_head_stride_words, void* o, float* lse, void* stream) {
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward supports d = 64 and 128");
+  if (int rc = check_common(ATTN_BF16, B, H, n, d, q8, k8, vt8, mask_kind, mask_bits,
+                            mask_row_words, mask_head_stride_words, 0))
+    return rc;
+  if (n % 16 != 0) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward needs n a multiple of 16");
+  if (!(q_scale > 0.0f) || !(k_scale > 0.0f) || !(v_scale > 0.0f) || !std::isfinite(q_scale) ||
+      !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return fail(ATTN_ERR_INVALID_ARG, "the FP8 scales must be finite and positive");
+  if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
+  if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  ea::AttnArgs a = make_args(B, H, n, d, c, q8, k8, vt8, mask_kind, mask_bits, mask_row_words,
+                             mask_head_stride_words, 0);
+  a.o_out = o;
+  a.lse = lse;
+  if (int rc = status_ptr(&a.status)) return rc;
+  std::string err;
+  int rc = ea::launch_fwd_fp8(a, vt8, q_scale, k_scale, v_scale, static_cast<cudaStream_t>(stream),
+                              err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
 int attn_merge(int dtype, int num_parts, int64_t rows, int d, const float* o_parts,
                const float* lse_parts, void* o, float* lse, void* stream) {
   if (dtype < ATTN_F32 || dtype > ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype");

@@ -69,6 +69,11 @@ int launch_bwd_tc(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err
 int launch_fwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
 int launch_bwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
 
+// FP8 forward: a.q, a.k are E4M3 [B*H][n][d], vt8 E4M3 [B*H][d][n] (V transposed), per-tensor
+// scales; a.o_out bfloat16.
+int launch_fwd_fp8(const AttnArgs& a, const void* vt8, float sq, float sk, float sv,
+                   cudaStream_t s, std::string& err);
+
 // O = sum_g exp(LSE_g - LSE) O_g, LSE = ln sum_g exp(LSE_g) over num_parts partial results
 // (float32 o_part [parts][rows][d], lse_part [parts][rows]); o in the output dtype.
 int launch_merge(int dtype_out, int num_parts, int64_t rows, int d, const float* o_part,

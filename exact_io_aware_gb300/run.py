@@ -45,6 +45,7 @@ def main(argv=None):
     ap.add_argument("--dropout", type=float, default=0.0, help="drop probability (0 = none)")
     ap.add_argument("--n-kv", type=int, default=0,
                     help="keys of a key/value cache (forward of --n query rows through attn_fwd_kv)")
+    ap.add_argument("--fp8", action="store_true", help="forward through attn_fwd_fp8 (E4M3 inputs)")
     ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
 
@@ -70,6 +71,8 @@ def main(argv=None):
     ea.load()
     if a.n_kv:
         return _run_kv(a, B, H, n, a.n_kv, d, dt, mask, c, kvb)
+    if a.fp8:
+        return _run_fp8(a, B, H, n, d, mask, c)
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     shape = (B, H, n, d)
@@ -112,6 +115,36 @@ def main(argv=None):
         print(json.dumps(out))
     else:
         print(" ".join(f"{k}={v:.4g}" if isinstance(v, float) else f"{k}={v}" for k, v in out.items()))
+    return 0 if status == ea.ATTN_OK else 1
+
+
+def _run_fp8(a, B, H, n, d, mask, c):
+    """FP8 forward on N(0,1) inputs quantized per tensor; time and TFLOP/s."""
+    import numpy as np
+    import torch
+
+    import exact_io_aware_gb300 as ea
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0)
+    xs = [torch.randn((B, H, n, d), device="cuda", generator=g) for _ in range(3)]
+    scales = [float(x.abs().max()) / 448.0 for x in xs]
+    q8, k8, v8 = ((x / s).to(torch.float8_e4m3fn) for x, s in zip(xs, scales))
+    vt8 = v8.transpose(2, 3).contiguous()
+    o = torch.empty((B, H, n, d), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty((B, H, n), device="cuda", dtype=torch.float32)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.iters + 1)]
+    for e in ev:
+        e[0].record()
+        ea.attn_fwd_fp8(q8, k8, vt8, c, *scales, mask=mask, o=o, lse=lse)
+        e[1].record()
+    torch.cuda.synchronize()
+    status = ea.attn_device_status()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
+    kappa = 0.5 if mask == "causal" else 1.0
+    out = {"workload": "fp8", "B": B, "H": H, "n": n, "d": d, "dtype": "e4m3", "mask": mask,
+           "fwd_ms": ms, "fwd_tflops": 4.0 * B * H * n * n * d * kappa / (ms / 1e3) / 1e12,
+           "status": status}
+    print(json.dumps(out) if a.json else " ".join(f"{k}={v}" for k, v in out.items()))
     return 0 if status == ea.ATTN_OK else 1
 
 

@@ -158,6 +158,28 @@ int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c,
                 int64_t mask_head_stride_words, int kv_block, int num_splits,
                 void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * FP8 forward: exact tiled attention with E4M3 operands on the tensor cores (kind::f8f6f4),
+ * bfloat16 output.  The inputs carry one scale each: Q = q_scale q8, K = k_scale k8 and
+ * V = v_scale vt8ᵀ, where
+ *   q8, k8  E4M3 [B][H][n][d]
+ *   vt8     E4M3 [B][H][d][n]: V transposed (the value columns are rows), so that the P V
+ *           product reads a K-major operand
+ * The scores are c·q_scale·k_scale·(q8·k8) accumulated in float32.  Each probability enters the
+ * P V product as an E4M3 value of 2^8 exp(s - m) (m the exact running maximum); the row sum
+ * keeps the unrounded values.  The output therefore differs from exact attention on the
+ * dequantized inputs by at most sum_j (2^-4 P_ij + 2^-18) |V_j| per element (the rounding of P),
+ * plus float32 and bfloat16 rounding.  lse is float32, natural log, of the scaled scores.
+ *   d: 64 or 128; n: a multiple of 16; masks as for attn_fwd; o: bfloat16 [B][H][n][d].
+ * The pages' FP8 forward (FlashAttention-3 on H100, "Bellek Duvarının Fiziği") adds block
+ * scaling and incoherent processing; this entry point takes one scale per tensor.
+ */
+int attn_fwd_fp8(int B, int H, int n, int d, float c,
+                 const void* q8, const void* k8, const void* vt8,
+                 float q_scale, float k_scale, float v_scale,
+                 int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                 int64_t mask_head_stride_words, void* o, float* lse, void* stream);
+
 /* The number of key shares attn_fwd_kv uses when num_splits = 0 on the current device. */
 int attn_fwd_kv_split_count(int dtype, int B, int H, int n_q, int n_kv, int d, int kv_block);
 
