@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_kv", "attn_fwd_kv_split_count",
-    "attn_fwd_fp8",
+    "attn_fwd_fp8", "attn_fp8_quantize", "attn_fwd_fp8_blocks",
     "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
@@ -93,6 +93,12 @@ def load():
     lib.attn_fwd_fp8.argtypes = [i32, i32, i32, i32, f32, vp, vp, vp, f32, f32, f32, i32, vp, i64,
                                  i64, vp, vp, vp]
     lib.attn_fwd_fp8.restype = i32
+    lib.attn_fwd_fp8_blocks.argtypes = [i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, i32, vp,
+                                        i64, i64, vp, vp, vp]
+    lib.attn_fwd_fp8_blocks.restype = i32
+    lib.attn_fp8_quantize.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                      vp, vp]
+    lib.attn_fp8_quantize.restype = i32
     u64 = ctypes.c_uint64
     lib.attn_fwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
                                      i32, f32, u64, vp, vp, vp]
@@ -264,6 +270,57 @@ def attn_fwd_fp8(q8, k8, vt8, c, q_scale, k_scale, v_scale, mask="none", mask_bi
     _check(load().attn_fwd_fp8(B, H, n, d, float(c), _ptr(q8), _ptr(k8), _ptr(vt8),
                                float(q_scale), float(k_scale), float(v_scale), kind, _ptr(bits),
                                row_words, hs, _ptr(o), _ptr(lse), _stream_ptr(stream)))
+    return o, lse
+
+
+def attn_fp8_quantize(q, k, v, signs=None, stream=None):
+    """Block quantization to E4M3 for ``attn_fwd_fp8_blocks``: q, k, v bf16/fp16 [B,H,n,d]
+    (d 64 or 128, n a multiple of 16); ``signs`` an int8 CUDA tensor of d entries turns on
+    incoherent processing of q and k.  Returns (q8, k8, vt8, q_scales, k_scales, v_scales):
+    E4M3 [B,H,n,d], [B,H,n,d], [B,H,d,n] and float32 [B,H,ceil(n/128)]."""
+    B, H, n, d = _shape(q, k, v)
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bfloat16 or float16")
+    if signs is not None:
+        if signs.dtype != torch.int8 or not signs.is_cuda or signs.numel() != d:
+            raise ValueError("signs must be an int8 CUDA tensor of d entries")
+        signs = signs.contiguous()
+    f8 = getattr(torch, "float8_e4m3fn", torch.uint8)
+    q8 = torch.empty((B, H, n, d), dtype=f8, device=q.device)
+    k8 = torch.empty((B, H, n, d), dtype=f8, device=q.device)
+    vt8 = torch.empty((B, H, d, n), dtype=f8, device=q.device)
+    nb = (n + 127) // 128
+    sq, sk, sv = (torch.empty((B, H, nb), dtype=torch.float32, device=q.device) for _ in range(3))
+    _check(load().attn_fp8_quantize(DTYPE_CODE[q.dtype], B, H, n, d, _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(signs), _ptr(q8), _ptr(k8), _ptr(vt8), _ptr(sq),
+                                    _ptr(sk), _ptr(sv), _stream_ptr(stream)))
+    return q8, k8, vt8, sq, sk, sv
+
+
+def attn_fwd_fp8_blocks(q8, k8, vt8, q_scales, k_scales, v_scales, c, mask="none",
+                        mask_bits=None, mask_head_stride_words=0, o=None, lse=None, stream=None):
+    """FP8 forward with one float32 scale per 128-row block of Q, K and V ([B,H,ceil(n/128)]
+    CUDA tensors, as ``attn_fp8_quantize`` returns them); returns (o bfloat16 [B,H,n,d], lse)."""
+    q8, k8, vt8 = (_fp8_bytes(t, nm) for t, nm in ((q8, "q8"), (k8, "k8"), (vt8, "vt8")))
+    if q8.dim() != 4 or k8.shape != q8.shape:
+        raise ValueError("q8 and k8 must be [B,H,n,d]")
+    B, H, n, d = q8.shape
+    if tuple(vt8.shape) != (B, H, d, n):
+        raise ValueError("vt8 must be [B,H,d,n] (V transposed)")
+    nb = (n + 127) // 128
+    for t, nm in ((q_scales, "q_scales"), (k_scales, "k_scales"), (v_scales, "v_scales")):
+        if (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()
+                or tuple(t.shape) != (B, H, nb)):
+            raise ValueError(f"{nm} must be a contiguous float32 CUDA tensor [B,H,ceil(n/128)]")
+    kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
+    if o is None:
+        o = torch.empty((B, H, n, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, n), dtype=torch.float32, device=q8.device)
+    _check(load().attn_fwd_fp8_blocks(B, H, n, d, float(c), _ptr(q8), _ptr(k8), _ptr(vt8),
+                                      _ptr(q_scales), _ptr(k_scales), _ptr(v_scales), kind,
+                                      _ptr(bits), row_words, hs, _ptr(o), _ptr(lse),
+                                      _stream_ptr(stream)))
     return o, lse
 
 

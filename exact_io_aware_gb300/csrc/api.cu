@@ -325,8 +325,65 @@ int attn_fwd_fp8(int B, int H, int n, int d, float c, const void* q8, const void
   a.lse = lse;
   if (int rc = status_ptr(&a.status)) return rc;
   std::string err;
-  int rc = ea::launch_fwd_fp8(a, vt8, q_scale, k_scale, v_scale, static_cast<cudaStream_t>(stream),
-                              err);
+  int rc = ea::launch_fwd_fp8(a, vt8, q_scale, k_scale, v_scale, nullptr, nullptr, nullptr,
+                              static_cast<cudaStream_t>(stream), err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
+int attn_fwd_fp8_blocks(int B, int H, int n, int d, float c, const void* q8, const void* k8,
+                        const void* vt8, const float* q_scales, const float* k_scales,
+                        const float* v_scales, int mask_kind, const uint32_t* mask_bits,
+                        int64_t mask_row_words, int64_t mask_head_stride_words, void* o,
+                        float* lse, void* stream) {
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward supports d = 64 and 128");
+  if (int rc = check_common(ATTN_BF16, B, H, n, d, q8, k8, vt8, mask_kind, mask_bits,
+                            mask_row_words, mask_head_stride_words, 0))
+    return rc;
+  if (n % 16 != 0) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward needs n a multiple of 16");
+  if (!q_scales || !k_scales || !v_scales) return fail(ATTN_ERR_INVALID_ARG, "null scale pointer");
+  if ((reinterpret_cast<uintptr_t>(q_scales) | reinterpret_cast<uintptr_t>(k_scales) |
+       reinterpret_cast<uintptr_t>(v_scales)) & 3u)
+    return fail(ATTN_ERR_ALIGNMENT, "scales must be 4-byte aligned");
+  if (!std::isfinite(c)) return fail(ATTN_ERR_INVALID_ARG, "c must be finite");
+  if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
+  if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return fail(ATTN_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  ea::AttnArgs a = make_args(B, H, n, d, c, q8, k8, vt8, mask_kind, mask_bits, mask_row_words,
+                             mask_head_stride_words, 0);
+  a.o_out = o;
+  a.lse = lse;
+  if (int rc = status_ptr(&a.status)) return rc;
+  std::string err;
+  int rc = ea::launch_fwd_fp8(a, vt8, 1.0f, 1.0f, 1.0f, q_scales, k_scales, v_scales,
+                              static_cast<cudaStream_t>(stream), err);
+  if (rc) return fail(rc, err);
+  return ATTN_OK;
+}
+
+int attn_fp8_quantize(int dtype, int B, int H, int n, int d, const void* q, const void* k,
+                      const void* v, const int8_t* signs, void* q8, void* k8, void* vt8,
+                      float* q_scales, float* k_scales, float* v_scales, void* stream) {
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16)
+    return fail(ATTN_ERR_UNSUPPORTED, "the FP8 quantization reads bf16 or fp16 inputs");
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 quantization supports d = 64 and 128");
+  if (B < 1 || H < 1 || n < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and n must be positive");
+  if (n % 16 != 0) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 quantization needs n a multiple of 16");
+  if (!q || !k || !v || !q8 || !k8 || !vt8 || !q_scales || !k_scales || !v_scales)
+    return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(vt8))
+    return fail(ATTN_ERR_ALIGNMENT, "tensors must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q_scales) | reinterpret_cast<uintptr_t>(k_scales) |
+       reinterpret_cast<uintptr_t>(v_scales)) & 3u)
+    return fail(ATTN_ERR_ALIGNMENT, "scales must be 4-byte aligned");
+  if (static_cast<int64_t>(B) * H > 65535)
+    return fail(ATTN_ERR_UNSUPPORTED, "B * H above 65535");
+  std::string err;
+  int rc = ea::launch_fp8_quantize(dtype == ATTN_BF16, B, H, n, d, q, k, v, signs, q8, k8, vt8,
+                                   q_scales, k_scales, v_scales, static_cast<cudaStream_t>(stream),
+                                   err);
   if (rc) return fail(rc, err);
   return ATTN_OK;
 }

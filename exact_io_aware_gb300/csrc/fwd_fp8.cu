@@ -7,9 +7,9 @@
 namespace ea {
 namespace fp8 {
 
-template <int D>
-int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, cudaStream_t s,
-        std::string& err) {
+template <int D, bool kBlocks>
+int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, const float* sq_blk,
+        const float* sk_blk, const float* sv_blk, cudaStream_t s, std::string& err) {
   using Cfg = Config<D>;
   const size_t smem = Cfg::smem_bytes(a.n, a.mask_kind);
   if (smem > static_cast<size_t>(kMaxDynSmem)) {
@@ -24,7 +24,7 @@ int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, cudaSt
     err = "cuTensorMapEncodeTiled rejected an FP8 tensor map";
     return -5;
   }
-  auto kern = fwd_fp8_kernel<D>;
+  auto kern = fwd_fp8_kernel<D, kBlocks>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
@@ -40,7 +40,10 @@ int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, cudaSt
            a.mask_head_stride_words,
            static_cast<__nv_bfloat16*>(a.o_out),
            a.lse,
-           a.status};
+           a.status,
+           sq_blk,
+           sk_blk,
+           sv_blk};
   dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   e = cudaGetLastError();
@@ -54,10 +57,15 @@ int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, cudaSt
 }  // namespace fp8
 
 int launch_fwd_fp8(const AttnArgs& a, const void* vt8, float sq, float sk, float sv,
-                   cudaStream_t s, std::string& err) {
+                   const float* sq_blk, const float* sk_blk, const float* sv_blk, cudaStream_t s,
+                   std::string& err) {
   switch (a.d) {
-    case 64: return fp8::run<64>(a, vt8, sq, sk, sv, s, err);
-    case 128: return fp8::run<128>(a, vt8, sq, sk, sv, s, err);
+    case 64:
+      return sk_blk ? fp8::run<64, true>(a, vt8, sq, sk, sv, sq_blk, sk_blk, sv_blk, s, err)
+                    : fp8::run<64, false>(a, vt8, sq, sk, sv, sq_blk, sk_blk, sv_blk, s, err);
+    case 128:
+      return sk_blk ? fp8::run<128, true>(a, vt8, sq, sk, sv, sq_blk, sk_blk, sv_blk, s, err)
+                    : fp8::run<128, false>(a, vt8, sq, sk, sv, sq_blk, sk_blk, sv_blk, s, err);
     default: err = "the FP8 forward supports d = 64 and 128"; return -2;
   }
 }

@@ -15,6 +15,13 @@
 // by sum_j (2^-4 p_ij + 2^-18) |V_j| / l_i (half an E4M3 ulp relative, or half the smallest
 // subnormal step).
 //
+// Block scaling (the FP8 variant the same page names for FlashAttention-3): with one scale per
+// 128-row block, sq_I of the query tile and sk_J of key block J make the score factor
+// c sq_I sk_J per block (a scalar per row and step); the value scale sv_J of block J enters
+// through the probabilities: P'_ij = 2^8 exp(score - m) r_J with r_J = sv_J / max_J sv_J <= 1,
+// added to the exponent as log2 r_J, and z is multiplied by max_J sv_J in the epilogue.  The
+// row sum takes each block's sum of P' divided by r_J, so l stays the sum of 2^8 exp(score - m).
+//
 // Layout and roles as the 16-bit kernel: one CTA owns two tiles of 128 query rows of one head;
 // warp 0 and 1 issue the MMAs of tile 0 and 1, warps 2-9 are the softmax (one query row per
 // lane), warp 10 the TMA producer.  Key blocks of 128; d in {64, 128}; no key split, no dropout.
@@ -47,6 +54,11 @@ struct Params {
   __nv_bfloat16* o;
   float* lse;
   uint32_t* status;
+  // Block scales [heads][ceil(n / 128)] (null: one scale per tensor, folded into sl2 and sv).
+  // With them sl2 is c log2(e) and sv is unused.
+  const float* sq_blk;
+  const float* sk_blk;
+  const float* sv_blk;
 };
 
 // Tiles of 8-bit elements use the 16-bit layouts with half as many columns: a row of C bytes
@@ -104,7 +116,7 @@ __device__ __forceinline__ uint32_t dense_step(int j, int nblk, int n, int pair_
   return w;
 }
 
-template <int D>
+template <int D, bool kBlocks>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_vt, Params p) {
@@ -319,6 +331,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.sl2 == 0.0f ? 1.17549435e-38f : p.sl2;  // c = 0: all weights equal
     const bool pos = sl2 > 0.0f;
     const float mv = pos ? -INFINITY : INFINITY;
+    constexpr bool blocks = kBlocks;
+    const int64_t sbase = static_cast<int64_t>(bh) * nblk;
+    float kq = sl2;      // score factor without the key block's scale
+    float vmax = p.sv;   // value scale of the epilogue
+    float l2vmax = 0.0f;
+    if (blocks) {
+      kq = sl2 * __ldg(p.sq_blk + sbase + min(pair * 2 + t, nblk - 1));
+      float mxv = 0.0f;
+      for (int jb = lane; jb < nblk; jb += 32) mxv = fmaxf(mxv, __ldg(p.sv_blk + sbase + jb));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mxv = fmaxf(mxv, __shfl_xor_sync(0xFFFFFFFFu, mxv, o));
+      vmax = mxv;
+      l2vmax = __log2f(mxv);
+    }
     float m = -INFINITY;  // exact running maximum, log2 units
     float l = 0.0f;       // running sum of 2^8 exp(score - m)
     uint32_t s_phase = 0;
@@ -333,6 +359,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t cls = (sw >> (16 + 2 * t)) & 3u;
       if (cls == kSkip) continue;
       const int key0 = static_cast<int>(sw & 0xFFFFu) * BN;
+      // this block's score factor kj, log2 r_J and 1 / r_J (loaded before the wait)
+      float kj = sl2, lr = 0.0f, inv_r = 1.0f;
+      if (blocks) {
+        const int jb = static_cast<int>(sw & 0xFFFFu);
+        kj = kq * __ldg(p.sk_blk + sbase + jb);
+        kj = pos ? fmaxf(kj, 1.17549435e-38f) : fminf(kj, -1.17549435e-38f);
+        lr = __log2f(__ldg(p.sv_blk + sbase + jb)) - l2vmax;
+        inv_r = ex2(-lr);
+      }
       ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
       if (!ok) break;
       s_phase ^= 1;
@@ -392,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         a0 = fmin3(a0, a1, fminf(a2, a3));
       }
-      const float mx = a0 == mv ? -INFINITY : a0 * sl2;
+      const float mx = a0 == mv ? -INFINITY : a0 * kj;
       float alpha = 1.0f;
       if (mx > m) {  // exact maximum: P never exceeds 2^8
         alpha = ex2(m - mx);
@@ -411,18 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       first = false;
-      // P = 2^8 exp2(s sl2 - m): the +8 in the exponent keeps small probabilities normal in E4M3
-      const float neg_mu = (m == -INFINITY) ? 0.0f : 8.0f - m;
+      // P = 2^8 r_J exp2(s kj - m): the +8 in the exponent keeps small probabilities normal in
+      // E4M3; r_J (block scales) rides along in the exponent
+      const float neg_mu = (m == -INFINITY) ? 0.0f : 8.0f - m + lr;
       float r0 = 0.0f, r1 = 0.0f, r2 = 0.0f, r3 = 0.0f;
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 64) {
         uint32_t pk[16];  // 64 keys, four per word
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float p0 = ex2(fmaf(sv[c0 + 4 * k], sl2, neg_mu));
-          const float p1 = ex2(fmaf(sv[c0 + 4 * k + 1], sl2, neg_mu));
-          const float p2 = ex2(fmaf(sv[c0 + 4 * k + 2], sl2, neg_mu));
-          const float p3 = ex2(fmaf(sv[c0 + 4 * k + 3], sl2, neg_mu));
+          const float p0 = ex2(fmaf(sv[c0 + 4 * k], kj, neg_mu));
+          const float p1 = ex2(fmaf(sv[c0 + 4 * k + 1], kj, neg_mu));
+          const float p2 = ex2(fmaf(sv[c0 + 4 * k + 2], kj, neg_mu));
+          const float p3 = ex2(fmaf(sv[c0 + 4 * k + 3], kj, neg_mu));
           r0 += p0;
           r1 += p1;
           r2 += p2;
@@ -431,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st16(tS + lane_off + c0 / 4, pk);
       }
-      l += (r0 + r1) + (r2 + r3);
+      l += ((r0 + r1) + (r2 + r3)) * inv_r;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -442,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pair_row0 + t * kRowsPerTile < n) {
       if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
       tc_fence_after();
-      const float inv = l > 0.0f ? p.sv / l : 0.0f;
+      const float inv = l > 0.0f ? vmax / l : 0.0f;
       if (ok) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(bh) * n + row) * D);
 #pragma unroll

@@ -71,8 +71,16 @@ int launch_bwd_f32(const AttnArgs& a, cudaStream_t s, std::string& err);
 
 // FP8 forward: a.q, a.k are E4M3 [B*H][n][d], vt8 E4M3 [B*H][d][n] (V transposed), per-tensor
 // scales; a.o_out bfloat16.
+// sq_blk, sk_blk, sv_blk: per-block scales [heads][ceil(n / 128)], or null for the scalars.
 int launch_fwd_fp8(const AttnArgs& a, const void* vt8, float sq, float sk, float sv,
-                   cudaStream_t s, std::string& err);
+                   const float* sq_blk, const float* sk_blk, const float* sv_blk, cudaStream_t s,
+                   std::string& err);
+
+// Block quantization of 16-bit Q, K, V to E4M3 (q8, k8 [heads][n][d], vt8 [heads][d][n]) with
+// float32 scales per 128 rows; signs (d entries, or null) turn on incoherent processing.
+int launch_fp8_quantize(bool bf16, int B, int H, int n, int d, const void* q, const void* k,
+                        const void* v, const int8_t* signs, void* q8, void* k8, void* vt8,
+                        float* sq, float* sk, float* sv, cudaStream_t s, std::string& err);
 
 // O = sum_g exp(LSE_g - LSE) O_g, LSE = ln sum_g exp(LSE_g) over num_parts partial results
 // (float32 o_part [parts][rows][d], lse_part [parts][rows]); o in the output dtype.

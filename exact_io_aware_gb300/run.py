@@ -46,6 +46,10 @@ def main(argv=None):
     ap.add_argument("--n-kv", type=int, default=0,
                     help="keys of a key/value cache (forward of --n query rows through attn_fwd_kv)")
     ap.add_argument("--fp8", action="store_true", help="forward through attn_fwd_fp8 (E4M3 inputs)")
+    ap.add_argument("--fp8-blocks", action="store_true",
+                    help="with --fp8: attn_fp8_quantize (timed apart) + attn_fwd_fp8_blocks")
+    ap.add_argument("--rotate", action="store_true",
+                    help="with --fp8-blocks: incoherent processing of Q and K")
     ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
 
@@ -127,23 +131,44 @@ def _run_fp8(a, B, H, n, d, mask, c):
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     xs = [torch.randn((B, H, n, d), device="cuda", generator=g) for _ in range(3)]
-    scales = [float(x.abs().max()) / 448.0 for x in xs]
-    q8, k8, v8 = ((x / s).to(torch.float8_e4m3fn) for x, s in zip(xs, scales))
-    vt8 = v8.transpose(2, 3).contiguous()
     o = torch.empty((B, H, n, d), device="cuda", dtype=torch.bfloat16)
     lse = torch.empty((B, H, n), device="cuda", dtype=torch.float32)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(a.iters + 1)]
-    for e in ev:
-        e[0].record()
-        ea.attn_fwd_fp8(q8, k8, vt8, c, *scales, mask=mask, o=o, lse=lse)
-        e[1].record()
-    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.iters + 1)]
+    quant_ms = None
+    if a.fp8_blocks:
+        xb = [x.to(torch.bfloat16) for x in xs]
+        signs = None
+        if a.rotate:
+            signs = (torch.randint(0, 2, (d,), device="cuda", generator=g) * 2 - 1).to(torch.int8)
+        ops = None
+        for e in ev:
+            e[0].record()
+            ops = ea.attn_fp8_quantize(*xb, signs=signs)
+            e[1].record()
+            ea.attn_fwd_fp8_blocks(*ops, c, mask=mask, o=o, lse=lse)
+            e[2].record()
+        torch.cuda.synchronize()
+        quant_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
+        ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev[1:]]))
+    else:
+        scales = [float(x.abs().max()) / 448.0 for x in xs]
+        q8, k8, v8 = ((x / s).to(torch.float8_e4m3fn) for x, s in zip(xs, scales))
+        vt8 = v8.transpose(2, 3).contiguous()
+        for e in ev:
+            e[0].record()
+            ea.attn_fwd_fp8(q8, k8, vt8, c, *scales, mask=mask, o=o, lse=lse)
+            e[1].record()
+        torch.cuda.synchronize()
+        ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
     status = ea.attn_device_status()
-    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
     kappa = 0.5 if mask == "causal" else 1.0
-    out = {"workload": "fp8", "B": B, "H": H, "n": n, "d": d, "dtype": "e4m3", "mask": mask,
+    out = {"workload": "fp8_blocks" if a.fp8_blocks else "fp8", "B": B, "H": H, "n": n, "d": d,
+           "dtype": "e4m3", "mask": mask, "rotate": bool(a.rotate),
            "fwd_ms": ms, "fwd_tflops": 4.0 * B * H * n * n * d * kappa / (ms / 1e3) / 1e12,
            "status": status}
+    if quant_ms is not None:
+        qbytes = 3 * B * H * n * d * 3 + 3 * 4 * B * H * ((n + 127) // 128)  # read 2 B, write 1 B
+        out.update(quant_ms=quant_ms, quant_gbs=qbytes / (quant_ms / 1e3) / 1e9)
     print(json.dumps(out) if a.json else " ".join(f"{k}={v}" for k, v in out.items()))
     return 0 if status == ea.ATTN_OK else 1
 

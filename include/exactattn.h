@@ -172,13 +172,59 @@ int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c,
  * plus float32 and bfloat16 rounding.  lse is float32, natural log, of the scaled scores.
  *   d: 64 or 128; n: a multiple of 16; masks as for attn_fwd; o: bfloat16 [B][H][n][d].
  * The pages' FP8 forward (FlashAttention-3 on H100, "Bellek Duvarının Fiziği") adds block
- * scaling and incoherent processing; this entry point takes one scale per tensor.
+ * scaling and incoherent processing: see attn_fp8_quantize and attn_fwd_fp8_blocks.  This
+ * entry point takes one scale per tensor.
  */
 int attn_fwd_fp8(int B, int H, int n, int d, float c,
                  const void* q8, const void* k8, const void* vt8,
                  float q_scale, float k_scale, float v_scale,
                  int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
                  int64_t mask_head_stride_words, void* o, float* lse, void* stream);
+
+/*
+ * Block quantization for the FP8 forward, with optional incoherent processing (the FP8 variant
+ * of "Bellek Duvarının Fiziği": per-block scales and random sign multipliers).
+ *
+ * A block is 128 consecutive rows of one (b, h) head of Q, K or V (the last one ragged).  Each
+ * block gets one float32 scale, absmax / 448 (1 for an all-zero block), and its codes are
+ * E4M3(x * (448 / absmax)) computed in float32, rounded to nearest even and saturated.
+ * With signs != NULL, Q and K are first incoherently processed: each row x becomes (x ∘ σ) H_d,
+ * σ_a = -1 where signs[a] < 0 else +1, H_d the order-d Walsh–Hadamard matrix (Sylvester's
+ * construction, entry (i, j) = (-1)^popcount(i & j)).  H_d H_dᵀ = d I, so the product of the
+ * processed Q and K is d Q Kᵀ; the factor 1/d is folded into Q's scales.  V is never rotated.
+ *   dtype      ATTN_BF16 or ATTN_F16 (type of q, k, v)
+ *   q, k, v    device [B][H][n][d], contiguous, 16-byte aligned
+ *   signs      device int8 [d], or NULL for no incoherent processing
+ *   q8, k8     device E4M3 [B][H][n][d] (outputs)
+ *   vt8        device E4M3 [B][H][d][n] (output): V's codes transposed
+ *   q_scales, k_scales, v_scales
+ *              device float32 [B][H][ceil(n / 128)] (outputs), 4-byte aligned
+ *   d: 64 or 128; n: a multiple of 16.  Asynchronous on `stream`; allocates nothing.
+ * Errors: ATTN_ERR_INVALID_ARG (non-positive sizes, null pointers), ATTN_ERR_UNSUPPORTED
+ * (dtype, d, n), ATTN_ERR_ALIGNMENT, ATTN_ERR_CUDA (launch).
+ */
+int attn_fp8_quantize(int dtype, int B, int H, int n, int d,
+                      const void* q, const void* k, const void* v, const int8_t* signs,
+                      void* q8, void* k8, void* vt8,
+                      float* q_scales, float* k_scales, float* v_scales, void* stream);
+
+/*
+ * FP8 forward with block scales: as attn_fwd_fp8, but Q, K and V carry one float32 scale per
+ * block of 128 rows, [B][H][ceil(n / 128)] device arrays as attn_fp8_quantize writes them:
+ * row i of Q is q_scales[i / 128] q8_i, key j is k_scales[j / 128] k8_j, value j is
+ * v_scales[j / 128] v8_j.  The score of (i, j) is c·q_scales[i/128]·k_scales[j/128]·(q8_i·k8_j).
+ * A value block's scale enters through the probabilities: those of key block J are rounded to
+ * E4M3 as 2^8 exp(s - m) r_J, r_J = v_scales[J] / max_J v_scales[J], and the output is
+ * multiplied by the largest scale at the end.  The output then differs from exact attention on
+ * the dequantized inputs by at most sum_j (2^-4 P_ij + 2^-18 / r_J(j)) |V_j| per element, plus
+ * float32 and bfloat16 rounding.  Other arguments, layouts and errors as for attn_fwd_fp8
+ * (ATTN_ERR_INVALID_ARG for a null scale pointer, ATTN_ERR_ALIGNMENT for a misaligned one).
+ */
+int attn_fwd_fp8_blocks(int B, int H, int n, int d, float c,
+                        const void* q8, const void* k8, const void* vt8,
+                        const float* q_scales, const float* k_scales, const float* v_scales,
+                        int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                        int64_t mask_head_stride_words, void* o, float* lse, void* stream);
 
 /* The number of key shares attn_fwd_kv uses when num_splits = 0 on the current device. */
 int attn_fwd_kv_split_count(int dtype, int B, int H, int n_q, int n_kv, int d, int kv_block);
