@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_kv", "attn_fwd_kv_split_count",
-    "attn_fwd_fp8", "attn_fp8_quantize", "attn_fwd_fp8_blocks",
+    "attn_fwd_fp8", "attn_fp8_quantize", "attn_fwd_fp8_blocks", "attn_fwd_vdim", "attn_bwd_vdim",
     "AttnError", "ATTN_OK", "ATTN_WARN_EMPTY_ROW", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
     "ATTN_ERR_ALIGNMENT", "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_DEVICE_TIMEOUT",
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
@@ -99,6 +99,12 @@ def load():
     lib.attn_fp8_quantize.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                       vp, vp]
     lib.attn_fp8_quantize.restype = i32
+    lib.attn_fwd_vdim.argtypes = [i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
+                                  i32, f32, ctypes.c_uint64, vp, vp, vp]
+    lib.attn_fwd_vdim.restype = i32
+    lib.attn_bwd_vdim.argtypes = [i32, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, i32,
+                                  vp, i64, i64, i32, f32, ctypes.c_uint64, vp, vp, vp, vp, sz, vp]
+    lib.attn_bwd_vdim.restype = i32
     u64 = ctypes.c_uint64
     lib.attn_fwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, i32, vp, i64, i64,
                                      i32, f32, u64, vp, vp, vp]
@@ -143,6 +149,18 @@ def _shape(q, k, v):
     return q.shape
 
 
+def _shape_v(q, k, v):
+    """(B, H, n, d, v_dim): q, k [B,H,n,d] and v [B,H,n,v_dim] (v_dim may differ from d)."""
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k must be [B,H,n,d] and v [B,H,n,v]")
+    if q.dtype not in DTYPE_CODE or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype among float32, float16, bfloat16")
+    for t in (q, k, v):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA tensors")
+    return (*q.shape, v.shape[3])
+
+
 def _mask_args(mask, mask_bits, mask_head_stride_words):
     kind = MASK_CODE[mask]
     if kind != 2:
@@ -156,15 +174,22 @@ def _mask_args(mask, mask_bits, mask_head_stride_words):
 
 def attn_fwd(q, k, v, c, mask="none", mask_bits=None, mask_head_stride_words=0, kv_block=0,
              o=None, lse=None, stream=None, dropout_p=0.0, seed=0):
-    """Forward pass; returns (o [B,H,n,d], lse [B,H,n] float32).  dropout_p > 0 drops
-    probabilities with the library's replayable mask for ``seed`` (attn_fwd_dropout)."""
-    B, H, n, d = _shape(q, k, v)
+    """Forward pass; returns (o [B,H,n,v], lse [B,H,n] float32).  dropout_p > 0 drops
+    probabilities with the library's replayable mask for ``seed`` (attn_fwd_dropout).  v may
+    be narrower or wider than q and k (attn_fwd_vdim)."""
+    B, H, n, d, v_dim = _shape_v(q, k, v)
     kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
     if o is None:
-        o = torch.empty_like(q)
+        o = torch.empty_like(v)
     if lse is None:
         lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
     lib = load()
+    if v_dim != d:
+        _check(lib.attn_fwd_vdim(DTYPE_CODE[q.dtype], B, H, n, d, v_dim, float(c), _ptr(q),
+                                 _ptr(k), _ptr(v), kind, _ptr(bits), row_words, hs,
+                                 int(kv_block), float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
+                                 _ptr(o), _ptr(lse), _stream_ptr(stream)))
+        return o, lse
     if dropout_p:
         _check(lib.attn_fwd_dropout(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k),
                                     _ptr(v), kind, _ptr(bits), row_words, hs, int(kv_block),
@@ -273,6 +298,16 @@ def attn_fwd_fp8(q8, k8, vt8, c, q_scale, k_scale, v_scale, mask="none", mask_bi
     return o, lse
 
 
+def attn_fwd_vdim(q, k, v, c, **kw):
+    """Forward with v [B,H,n,v] of its own width (the same call as attn_fwd)."""
+    return attn_fwd(q, k, v, c, **kw)
+
+
+def attn_bwd_vdim(q, k, v, o, lse, do, c, **kw):
+    """Backward with v, o, do [B,H,n,v] of their own width (the same call as attn_bwd)."""
+    return attn_bwd(q, k, v, o, lse, do, c, **kw)
+
+
 def attn_fp8_quantize(q, k, v, signs=None, stream=None):
     """Block quantization to E4M3 for ``attn_fwd_fp8_blocks``: q, k, v bf16/fp16 [B,H,n,d]
     (d 64 or 128, n a multiple of 16); ``signs`` an int8 CUDA tensor of d entries turns on
@@ -368,8 +403,9 @@ def attn_bwd(q, k, v, o, lse, do, c, mask="none", mask_bits=None, mask_head_stri
              kv_block=0, dq=None, dk=None, dv=None, workspace=None, stream=None, dropout_p=0.0,
              seed=0):
     """Backward pass (vector-Jacobian product for upstream ``do``); returns (dq, dk, dv).
-    dropout_p and seed must be those of the forward (attn_bwd_dropout replays its mask)."""
-    B, H, n, d = _shape(q, k, v)
+    dropout_p and seed must be those of the forward (attn_bwd_dropout replays its mask).
+    v, o, do and dv may be narrower or wider than q and k (attn_bwd_vdim)."""
+    B, H, n, d, v_dim = _shape_v(q, k, v)
     kind, bits, row_words, hs = _mask_args(mask, mask_bits, mask_head_stride_words)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -378,6 +414,14 @@ def attn_bwd(q, k, v, o, lse, do, c, mask="none", mask_bits=None, mask_head_stri
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     lib = load()
+    if v_dim != d:
+        _check(lib.attn_bwd_vdim(DTYPE_CODE[q.dtype], B, H, n, d, v_dim, float(c), _ptr(q),
+                                 _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits),
+                                 row_words, hs, int(kv_block), float(dropout_p),
+                                 int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dq), _ptr(dk), _ptr(dv),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream_ptr(stream)))
+        return dq, dk, dv
     if dropout_p:
         _check(lib.attn_bwd_dropout(DTYPE_CODE[q.dtype], B, H, n, d, float(c), _ptr(q), _ptr(k),
                                     _ptr(v), _ptr(o), _ptr(lse), _ptr(do), kind, _ptr(bits),
@@ -455,5 +499,6 @@ class _Attention(torch.autograd.Function):
 
 def attention(q, k, v, c, mask="none", mask_bits=None, kv_block=0, dropout_p=0.0, seed=0):
     """Differentiable exact attention O = softmax(c QKᵀ + mask) V, with optional dropout on
-    the probabilities (the backward replays the forward's mask for ``seed``)."""
+    the probabilities (the backward replays the forward's mask for ``seed``); v may have its
+    own width (q, k [B,H,n,d], v [B,H,n,v])."""
     return _Attention.apply(q, k, v, c, mask, mask_bits, kv_block, dropout_p, seed)

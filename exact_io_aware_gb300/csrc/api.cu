@@ -144,6 +144,7 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.H = H;
   a.n = n;
   a.d = d;
+  a.v_dim = d;
   a.c = c;
   a.q = q;
   a.k = k;
@@ -156,6 +157,13 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.num_splits = 1;
   a.nk = n;
   return a;
+}
+
+// Value width v of V, O, dO and dV: v = d, or (d, v) one of the pairs with instantiated kernels.
+int check_vdim(int d, int v_dim) {
+  if (v_dim == d) return ATTN_OK;
+  if ((d == 64 && v_dim == 128) || (d == 128 && v_dim == 64)) return ATTN_OK;
+  return fail(ATTN_ERR_UNSUPPORTED, "value width v != d is supported for (d, v) = (64, 128) and (128, 64)");
 }
 
 // One warp waits, with the library's bounded wait, on an mbarrier that nothing arrives on.
@@ -193,7 +201,7 @@ int set_dropout(float p_drop, uint64_t seed, ea::AttnArgs& a) {
 
 // Every forward entry point: nq query rows against nk keys (nk = nq for square attention),
 // optional dropout, and a key split of `splits` shares (1 = one pass straight into o, lse).
-int fwd_general(int dtype, int B, int H, int nq, int nk, int d, float c, const void* q,
+int fwd_general(int dtype, int B, int H, int nq, int nk, int d, int v_dim, float c, const void* q,
                 const void* k, const void* v, int mask_kind, const uint32_t* mask_bits,
                 int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                 float p_drop, uint64_t seed, int splits, void* o, float* lse, void* workspace,
@@ -202,6 +210,7 @@ int fwd_general(int dtype, int B, int H, int nq, int nk, int d, float c, const v
   if (int rc = check_common(dtype, B, H, nq, d, q, k, v, mask_kind, mask_bits, mask_row_words,
                             mask_head_stride_words, kv_block, nk))
     return rc;
+  if (int rc = check_vdim(d, v_dim)) return rc;
   if (!o || !lse) return fail(ATTN_ERR_INVALID_ARG, "null output pointer");
   if (!aligned16(o)) return fail(ATTN_ERR_ALIGNMENT, "o must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
@@ -209,11 +218,12 @@ int fwd_general(int dtype, int B, int H, int nq, int nk, int d, float c, const v
   ea::AttnArgs a = make_args(B, H, nq, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                              mask_head_stride_words, kv_block);
   a.nk = nk;
+  a.v_dim = v_dim;
   a.o_out = o;
   a.lse = lse;
   if (int rc = set_dropout(p_drop, seed, a)) return rc;
   if (splits > 1) {
-    const size_t need = split_ws_bytes(B, H, nq, d, splits);
+    const size_t need = split_ws_bytes(B, H, nq, v_dim, splits);
     if (!workspace || workspace_bytes < need)
       return fail(ATTN_ERR_WORKSPACE,
                   "workspace missing or smaller than attn_fwd_split_workspace_bytes");
@@ -222,7 +232,7 @@ int fwd_general(int dtype, int B, int H, int nq, int nk, int d, float c, const v
     a.num_splits = splits;
     a.o_part = static_cast<float*>(workspace);
     a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          split_part_bytes(B, H, nq, d, splits));
+                                          split_part_bytes(B, H, nq, v_dim, splits));
   }
   if (int rc = status_ptr(&a.status)) return rc;
   std::string err;
@@ -231,7 +241,7 @@ int fwd_general(int dtype, int B, int H, int nq, int nk, int d, float c, const v
                              : ea::launch_fwd_tc(dtype == ATTN_BF16, a, s, err);
   if (rc) return fail(rc, err);
   if (splits > 1) {
-    rc = ea::launch_merge(dtype, splits, static_cast<int64_t>(B) * H * nq, d, a.o_part,
+    rc = ea::launch_merge(dtype, splits, static_cast<int64_t>(B) * H * nq, v_dim, a.o_part,
                           a.lse_part, o, lse, a.status, s, err);
     if (rc) return fail(rc, err);
   }
@@ -245,7 +255,7 @@ extern "C" {
 int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
              const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
              int64_t mask_head_stride_words, int kv_block, void* o, float* lse, void* stream) {
-  return fwd_general(dtype, B, H, n, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+  return fwd_general(dtype, B, H, n, n, d, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                      mask_head_stride_words, kv_block, 0.0f, 0, 1, o, lse, nullptr, 0, stream);
 }
 
@@ -253,7 +263,7 @@ int attn_fwd_dropout(int dtype, int B, int H, int n, int d, float c, const void*
                      const void* v, int mask_kind, const uint32_t* mask_bits,
                      int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                      float p_drop, uint64_t seed, void* o, float* lse, void* stream) {
-  return fwd_general(dtype, B, H, n, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+  return fwd_general(dtype, B, H, n, n, d, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                      mask_head_stride_words, kv_block, p_drop, seed, 1, o, lse, nullptr, 0,
                      stream);
 }
@@ -283,7 +293,7 @@ int attn_fwd_split(int dtype, int B, int H, int n, int d, float c, const void* q
     return fail(ATTN_ERR_INVALID_ARG, "num_splits must be 0 (library choice) or 1..32");
   if (B < 1 || H < 1 || n < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and n must be positive");
   const int splits = num_splits ? num_splits : auto_splits(dtype, B, H, n, n, kv_block);
-  return fwd_general(dtype, B, H, n, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
+  return fwd_general(dtype, B, H, n, n, d, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                      mask_head_stride_words, kv_block, 0.0f, 0, splits, o, lse, workspace,
                      workspace_bytes, stream);
 }
@@ -298,7 +308,7 @@ int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c, cons
   if (B < 1 || H < 1 || n_q < 1 || n_kv < 1)
     return fail(ATTN_ERR_INVALID_ARG, "B, H, n_q and n_kv must be positive");
   const int splits = num_splits ? num_splits : auto_splits(dtype, B, H, n_q, n_kv, kv_block);
-  return fwd_general(dtype, B, H, n_q, n_kv, d, c, q, k, v, mask_kind, mask_bits,
+  return fwd_general(dtype, B, H, n_q, n_kv, d, d, c, q, k, v, mask_kind, mask_bits,
                      mask_row_words, mask_head_stride_words, kv_block, 0.0f, 0, splits, o, lse,
                      workspace, workspace_bytes, stream);
 }
@@ -419,7 +429,7 @@ size_t attn_bwd_workspace_bytes(int dtype, int B, int H, int n, int d) {
 
 namespace {
 
-int bwd_impl(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
+int bwd_impl(int dtype, int B, int H, int n, int d, int v_dim, float c, const void* q, const void* k,
              const void* v, const void* o, const float* lse, const void* d_o, int mask_kind,
              const uint32_t* mask_bits, int64_t mask_row_words, int64_t mask_head_stride_words,
              int kv_block, float p_drop, uint64_t seed, void* dq, void* dk, void* dv,
@@ -427,6 +437,7 @@ int bwd_impl(int dtype, int B, int H, int n, int d, float c, const void* q, cons
   if (int rc = check_common(dtype, B, H, n, d, q, k, v, mask_kind, mask_bits, mask_row_words,
                             mask_head_stride_words, kv_block))
     return rc;
+  if (int rc = check_vdim(d, v_dim)) return rc;
   if (!o || !lse || !d_o) return fail(ATTN_ERR_INVALID_ARG, "null o, lse or d_o");
   if (!dq || !dk || !dv) return fail(ATTN_ERR_INVALID_ARG, "null gradient pointer");
   if (!aligned16(o) || !aligned16(d_o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -439,6 +450,7 @@ int bwd_impl(int dtype, int B, int H, int n, int d, float c, const void* q, cons
   if (!aligned16(workspace)) return fail(ATTN_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
   ea::AttnArgs a = make_args(B, H, n, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                              mask_head_stride_words, kv_block);
+  a.v_dim = v_dim;
   a.o = o;
   a.lse = const_cast<float*>(lse);
   a.d_o = d_o;
@@ -466,7 +478,7 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
              const uint32_t* mask_bits, int64_t mask_row_words, int64_t mask_head_stride_words,
              int kv_block, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
              void* stream) {
-  return bwd_impl(dtype, B, H, n, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
+  return bwd_impl(dtype, B, H, n, d, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
                   mask_row_words, mask_head_stride_words, kv_block, 0.0f, 0, dq, dk, dv,
                   workspace, workspace_bytes, stream);
 }
@@ -477,7 +489,27 @@ int attn_bwd_dropout(int dtype, int B, int H, int n, int d, float c, const void*
                      int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                      float p_drop, uint64_t seed, void* dq, void* dk, void* dv, void* workspace,
                      size_t workspace_bytes, void* stream) {
-  return bwd_impl(dtype, B, H, n, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
+  return bwd_impl(dtype, B, H, n, d, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
+                  mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, dq, dk, dv,
+                  workspace, workspace_bytes, stream);
+}
+
+int attn_fwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c, const void* q,
+                  const void* k, const void* v, int mask_kind, const uint32_t* mask_bits,
+                  int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
+                  float p_drop, uint64_t seed, void* o, float* lse, void* stream) {
+  return fwd_general(dtype, B, H, n, n, d, v_dim, c, q, k, v, mask_kind, mask_bits,
+                     mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, 1, o, lse,
+                     nullptr, 0, stream);
+}
+
+int attn_bwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c, const void* q,
+                  const void* k, const void* v, const void* o, const float* lse, const void* d_o,
+                  int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                  int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  return bwd_impl(dtype, B, H, n, d, v_dim, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
                   mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, dq, dk, dv,
                   workspace, workspace_bytes, stream);
 }

@@ -9,7 +9,7 @@
 namespace ea {
 namespace aux {
 
-// One warp per row; rows = B*H*n.  Lanes stride over the d columns.
+// One warp per row; rows = B*H*n.  Lanes stride over the d columns (the value width).
 __global__ void __launch_bounds__(256) pre_kernel(const float* __restrict__ O,
                                                   const float* __restrict__ G,
                                                   float* __restrict__ Dv, int64_t rows, int d) {
@@ -38,7 +38,7 @@ inline int grid_for(int64_t work, int per_block) {
 int launch_bwd_pre_f32(const AttnArgs& a, float* D, cudaStream_t s, std::string& err) {
   const int64_t rows = static_cast<int64_t>(a.B) * a.H * a.n;
   aux::pre_kernel<<<aux::grid_for(rows, 8), 256, 0, s>>>(
-      static_cast<const float*>(a.o), static_cast<const float*>(a.d_o), D, rows, a.d);
+      static_cast<const float*>(a.o), static_cast<const float*>(a.d_o), D, rows, a.v_dim);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     err = std::string("backward preprocessing launch: ") + cudaGetErrorString(e);

@@ -79,32 +79,35 @@ __host__ __device__ constexpr int packed_col(int c) {
   return (c / (BQ / 2)) * (BQ / 2) + (c % (BQ / 2)) / 2;
 }
 
-template <int D>
+// D: width of Q, K, dK rows; DV: width of V, dO, dV rows (the value width).
+template <int D, int DV>
 struct Config {
-  using TK = Tile<kKeys, D>;  // K, V (and dK, dV staging)
-  using TQ = Tile<BQ, D>;     // Q, dO stages
+  using TK = Tile<kKeys, D>;   // K (and dK staging)
+  using TV = Tile<kKeys, DV>;  // V (and dV staging)
+  using TQ = Tile<BQ, D>;      // Q stages
+  using TG = Tile<BQ, DV>;     // dO stages
   // tensor-memory columns: S, dP, dV, dK
   static constexpr int kColS = 0;
   static constexpr int kColDP = BQ;
   static constexpr int kColDV = 2 * BQ;
-  static constexpr int kColDK = kColDV + pad32(D);
+  static constexpr int kColDK = kColDV + pad32(DV);
   static constexpr int kTmemCols = kColDK + pad32(D);
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   static constexpr int kTmemAlloc = kTmemCols <= 256 ? 256 : 512;
   // shared memory: K, V, then NS stages of (Q, dO, LSE, D), the step table, and (bitmap masks)
   // each stage's allowed-key words
   static constexpr int kBudget = 227 * 1024 - 2048;
-  static constexpr int kStage = 2 * TQ::kBytes + 2 * BQ * 4;
+  static constexpr int kStage = TQ::kBytes + TG::kBytes + 2 * BQ * 4;
   static constexpr int kMaxStepBytes = 4 * 1024;
-  static constexpr int kFixed = 2 * TK::kBytes;
+  static constexpr int kFixed = TK::kBytes + TV::kBytes;
   static constexpr int kFit = (kBudget - kFixed - kMaxStepBytes - 4 * BQ * 16) / kStage;
   static constexpr int NS = kFit > 4 ? 4 : kFit;
   static_assert(NS >= 2, "need two query stages");
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + TK::kBytes;
-  static constexpr int kOffQ = kOffV + TK::kBytes;
+  static constexpr int kOffQ = kOffV + TV::kBytes;
   static constexpr int kOffG = kOffQ + NS * TQ::kBytes;
-  static constexpr int kOffL = kOffG + NS * TQ::kBytes;  // [NS][BQ] LSE (log2 units)
+  static constexpr int kOffL = kOffG + NS * TG::kBytes;  // [NS][BQ] LSE (log2 units)
   static constexpr int kOffD = kOffL + NS * BQ * 4;      // [NS][BQ] D
   static constexpr int kOffSteps = kOffD + NS * BQ * 4;
   __host__ __device__ static constexpr int off_bits(int n) {
@@ -158,15 +161,17 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   }
 }
 
-template <bool kBf16, int D, bool kDrop>
+template <bool kBf16, int D, int DV, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                   BwdParams p) {
-  using C = Config<D>;
+  using C = Config<D, DV>;
   using TK = typename C::TK;
+  using TV = typename C::TV;
   using TQ = typename C::TQ;
+  using TG = typename C::TG;
   constexpr int NS = C::NS;
 
   extern __shared__ uint8_t smem_raw[];
@@ -275,26 +280,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_g);
-      mbar_arrive_expect_tx(&bars.kv_full, 2 * TK::kBytes);
+      mbar_arrive_expect_tx(&bars.kv_full, TK::kBytes + TV::kBytes);
 #pragma unroll
-      for (int b = 0; b < TK::L::kBoxes; ++b) {
+      for (int b = 0; b < TK::L::kBoxes; ++b)
         tma_load_3d(sK + b * TK::kBoxBytes, &tm_k, &bars.kv_full, b * TK::L::kBoxCols, key0, bh);
-        tma_load_3d(sV + b * TK::kBoxBytes, &tm_v, &bars.kv_full, b * TK::L::kBoxCols, key0, bh);
-      }
+#pragma unroll
+      for (int b = 0; b < TV::L::kBoxes; ++b)
+        tma_load_3d(sV + b * TV::kBoxBytes, &tm_v, &bars.kv_full, b * TV::L::kBoxCols, key0, bh);
     }
     for (int i = 0; i < nsteps; ++i) {
       const int s = i % NS;
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
       if (!mbar_wait_spin(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.qdo_full[s], 2 * TQ::kBytes);
+        mbar_arrive_expect_tx(&bars.qdo_full[s], TQ::kBytes + TG::kBytes);
 #pragma unroll
-        for (int b = 0; b < TQ::L::kBoxes; ++b) {
+        for (int b = 0; b < TQ::L::kBoxes; ++b)
           tma_load_3d(sQ + s * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.qdo_full[s],
                       b * TQ::L::kBoxCols, q0, bh);
-          tma_load_3d(sG + s * TQ::kBytes + b * TQ::kBoxBytes, &tm_g, &bars.qdo_full[s],
-                      b * TQ::L::kBoxCols, q0, bh);
-        }
+#pragma unroll
+        for (int b = 0; b < TG::L::kBoxes; ++b)
+          tma_load_3d(sG + s * TG::kBytes + b * TG::kBoxBytes, &tm_g, &bars.qdo_full[s],
+                      b * TG::L::kBoxCols, q0, bh);
       }
       if (lane == 0) {
         // rows q0 .. q0+BQ-1 of the row table (always inside the padded table)
@@ -326,11 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issues.  Operand descriptors are built once per buffer: a 16-element step or a ring
     // stage only adds a constant to the start-address field.
     constexpr uint32_t id_s = idesc_f16(128, BQ, kBf16 ? 1 : 0, 0, 0);  // Sᵀ, dPᵀ
-    constexpr uint32_t id_kv = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);  // dV, dK
+    constexpr uint32_t id_dk = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dK
+    constexpr uint32_t id_dv = idesc_f16(128, DV, kBf16 ? 1 : 0, 0, 1);  // dV
     constexpr uint64_t kStage = TQ::kBytes >> 4;
-    const uint64_t dk = TK::desc_k(smem_u32(sK), 0), dv = TK::desc_k(smem_u32(sV), 0);
-    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TQ::desc_k(smem_u32(sG), 0);
-    const uint64_t dqmn0 = TQ::desc_mn(smem_u32(sQ), 0), dgmn0 = TQ::desc_mn(smem_u32(sG), 0);
+    constexpr uint64_t kStageG = TG::kBytes >> 4;
+    const uint64_t dk = TK::desc_k(smem_u32(sK), 0), dv = TV::desc_k(smem_u32(sV), 0);
+    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TG::desc_k(smem_u32(sG), 0);
+    const uint64_t dqmn0 = TQ::desc_mn(smem_u32(sQ), 0), dgmn0 = TG::desc_mn(smem_u32(sG), 0);
     bool ok = mbar_wait_spin_warp(&bars.kv_full, 0, p.status, 22);
     auto wait_qdo = [&](int i) -> bool {
       return mbar_wait_spin_warp(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
@@ -346,11 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     auto issue_dp = [&](int i) {
-      const uint64_t dg = dg0 + static_cast<uint64_t>(i % NS) * kStage;
+      const uint64_t dg = dg0 + static_cast<uint64_t>(i % NS) * kStageG;
       if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, dv + TK::k_step(kk), dg + TQ::k_step(kk), id_s, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::kColDP, dv + TV::k_step(kk), dg + TG::k_step(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars.dp_full);
       }
       __syncwarp();
@@ -368,12 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_spin_warp(&bars.p_full, i & 1, p.status, 24);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t dgmn = dgmn0 + static_cast<uint64_t>(s) * kStage;
+      const uint64_t dgmn = dgmn0 + static_cast<uint64_t>(s) * kStageG;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), dgmn + TQ::mn_step(kk),
-                 id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), dgmn + TG::mn_step(kk),
+                 id_dv, (i > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
       const bool more = i + 1 < nsteps;
@@ -391,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
           mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(16 * kk), dqmn + TQ::mn_step(kk),
-                 id_kv, (i > 0 || kk > 0) ? 1u : 0u);
+                 id_dk, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.qdo_empty[s]);
       }
       __syncwarp();
@@ -541,25 +550,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = mbar_wait_spin(&bars.kv_done, 0, p.status, 31);
       tc_fence_after();
       if (ok) {
+        // dV (DV columns) into V's tile, then dK (D columns) into K's tile
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t rv[16], rk[16];
+        for (int c0 = 0; c0 < DV; c0 += 16) {
+          uint32_t rv[16];
           if (nsteps > 0) {
             tmem_ld16(tmem + C::kColDV + lane_off + c0, rv);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) rv[k] = 0u;
+          }
+          uint32_t pv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pv[k] = pack2<kBf16>(dvs * __uint_as_float(rv[2 * k]), dvs * __uint_as_float(rv[2 * k + 1]));
+          *reinterpret_cast<uint4*>(sV + TV::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+          *reinterpret_cast<uint4*>(sV + TV::offset(r, c0 + 8)) = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t rk[16];
+          if (nsteps > 0) {
             tmem_ld16(tmem + C::kColDK + lane_off + c0, rk);
             tmem_wait_ld();
           } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) rv[k] = rk[k] = 0u;
+            for (int k = 0; k < 16; ++k) rk[k] = 0u;
           }
-          uint32_t pv[8], pkk[8];
+          uint32_t pkk[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            pv[k] = pack2<kBf16>(dvs * __uint_as_float(rv[2 * k]), dvs * __uint_as_float(rv[2 * k + 1]));
+          for (int k = 0; k < 8; ++k)
             pkk[k] = pack2<kBf16>(p.c * __uint_as_float(rk[2 * k]), p.c * __uint_as_float(rk[2 * k + 1]));
-          }
-          *reinterpret_cast<uint4*>(sV + TK::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-          *reinterpret_cast<uint4*>(sV + TK::offset(r, c0 + 8)) = make_uint4(pv[4], pv[5], pv[6], pv[7]);
           *reinterpret_cast<uint4*>(sK + TK::offset(r, c0)) = make_uint4(pkk[0], pkk[1], pkk[2], pkk[3]);
           *reinterpret_cast<uint4*>(sK + TK::offset(r, c0 + 8)) =
               make_uint4(pkk[4], pkk[5], pkk[6], pkk[7]);
@@ -569,10 +591,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(2, 128);
       if (ok && r == 0) {
 #pragma unroll
-        for (int b = 0; b < TK::L::kBoxes; ++b) {
+        for (int b = 0; b < TK::L::kBoxes; ++b)
           tma_store_3d(&tm_dk, sK + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
-          tma_store_3d(&tm_dv, sV + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
-        }
+#pragma unroll
+        for (int b = 0; b < TV::L::kBoxes; ++b)
+          tma_store_3d(&tm_dv, sV + b * TV::kBoxBytes, b * TV::L::kBoxCols, key0, bh);
         tma_store_commit();
         tma_store_wait_all();
       }

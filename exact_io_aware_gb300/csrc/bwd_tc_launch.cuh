@@ -10,10 +10,10 @@ namespace bwd {
 
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 
-template <bool kBf16, int D, bool kDrop>
+template <bool kBf16, int D, int DV, bool kDrop>
 int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
-  using Cfg = Config<D>;
-  using QCfg = dq::Config<D>;
+  using Cfg = Config<D, DV>;
+  using QCfg = dq::Config<D, DV>;
   const bool bitmap = a.mask_kind == kMaskBitmap;
   const size_t smem = Cfg::smem_bytes(a.n, bitmap);
   const size_t qsmem = QCfg::smem_bytes(a.n, bitmap);
@@ -23,13 +23,14 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   }
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;
   constexpr uint32_t bc = RowLayout<D>::kBoxCols;
+  constexpr uint32_t bcv = RowLayout<DV>::kBoxCols;
   CUtensorMap tq, tk, tv, tg, tdk, tdv, tdq;
   if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, 128, bc) ||
-      !encode_tile_map(&tg, a.d_o, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tg, a.d_o, kBf16, heads, a.n, DV, 128, bcv) ||
       !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, 128, bc) ||
-      !encode_tile_map(&tv, a.v, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tv, a.v, kBf16, heads, a.n, DV, 128, bcv) ||
       !encode_tile_map(&tdk, a.dk, kBf16, heads, a.n, D, 128, bc) ||
-      !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, DV, 128, bcv) ||
       !encode_tile_map(&tdq, a.dq, kBf16, heads, a.n, D, 128, bc)) {
     err = "cuTensorMapEncodeTiled rejected a backward tensor map";
     return -5;
@@ -41,7 +42,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   p.drop = a.drop;
   const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
   // the dQ kernel writes the row table the dK/dV kernel reads
-  auto qkern = dq::dq_tc_kernel<kBf16, D, kDrop>;
+  auto qkern = dq::dq_tc_kernel<kBf16, D, DV, kDrop>;
   cudaError_t e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(qsmem));
   if (e == cudaSuccess) {
@@ -52,7 +53,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
     err = std::string("dQ launch: ") + cudaGetErrorString(e);
     return -5;
   }
-  auto kern = bwd_tc_kernel<kBf16, D, kDrop>;
+  auto kern = bwd_tc_kernel<kBf16, D, DV, kDrop>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e == cudaSuccess) {
@@ -66,12 +67,12 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   return 0;
 }
 
-// Instantiations with and without dropout for one head dimension.
-template <int D>
+// Instantiations with and without dropout for one (key width, value width) pair.
+template <int D, int DV = D>
 int run_d(bool bf16, const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   if (a.dropout)
-    return bf16 ? run<true, D, true>(a, table, s, err) : run<false, D, true>(a, table, s, err);
-  return bf16 ? run<true, D, false>(a, table, s, err) : run<false, D, false>(a, table, s, err);
+    return bf16 ? run<true, D, DV, true>(a, table, s, err) : run<false, D, DV, true>(a, table, s, err);
+  return bf16 ? run<true, D, DV, false>(a, table, s, err) : run<false, D, DV, false>(a, table, s, err);
 }
 
 }  // namespace bwd

@@ -60,10 +60,13 @@ using bwd::packed_col;
 using bwd::pad32;
 using bwd::unpack2;
 
-template <int D>
+// D: width of Q, K, dQ rows; DV: width of V, dO rows (the value width).
+template <int D, int DV>
 struct Config {
-  using TQ = Tile<kRows, D>;  // Q, dO (and dQ staging)
-  using TK = Tile<BN, D>;     // K, V stages
+  using TQ = Tile<kRows, D>;   // Q (and dQ staging)
+  using TG = Tile<kRows, DV>;  // dO
+  using TK = Tile<BN, D>;      // K stages
+  using TV = Tile<BN, DV>;     // V stages
   // tensor-memory columns: S, dP buffers, dQ
   static constexpr int kColS = 0;
   static constexpr int kColDP = BN;  // buffer b at BN + b * BN
@@ -72,17 +75,19 @@ struct Config {
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   static constexpr int kTmemAlloc = 512;
   static constexpr int kBudget = 227 * 1024 - 2048;  // dynamic limit less alignment slack
-  static constexpr int kFixed = 2 * TQ::kBytes;
+  static constexpr int kFixed = TQ::kBytes + TG::kBytes;
   static constexpr int kStepReserve = 1024;  // smallest step table kept room for (bitmap masks)
-  static constexpr int kSlots = (kBudget - kFixed - kStepReserve) / TK::kBytes;
-  static constexpr int NSV = kSlots / 2 > 4 ? 4 : kSlots / 2;
-  static constexpr int NSK = kSlots - NSV > 4 ? 4 : kSlots - NSV;
+  static constexpr int kAvail = kBudget - kFixed - kStepReserve;
+  static constexpr int kPairs = kAvail / (TK::kBytes + TV::kBytes);
+  static constexpr int NSV = kPairs > 4 ? 4 : kPairs;
+  static constexpr int kKFit = (kAvail - NSV * TV::kBytes) / TK::kBytes;
+  static constexpr int NSK = kKFit > 4 ? 4 : kKFit;
   static_assert(NSV >= 2 && NSK >= 2, "need two key and two value stages");
   static constexpr int kOffQ = 0;
   static constexpr int kOffG = kOffQ + TQ::kBytes;
-  static constexpr int kOffK = kOffG + TQ::kBytes;
+  static constexpr int kOffK = kOffG + TG::kBytes;
   static constexpr int kOffV = kOffK + NSK * TK::kBytes;
-  static constexpr int kOffSteps = kOffV + NSV * TK::kBytes;
+  static constexpr int kOffSteps = kOffV + NSV * TV::kBytes;
   // Only a bitmap mask needs the step table; the walk under the other masks is computed.
   static size_t smem_bytes(int n, bool bitmap) {
     return 1024 + kOffSteps + (bitmap ? 4 * static_cast<size_t>((n + BN - 1) / BN) : 0);
@@ -99,14 +104,16 @@ struct Barriers {
   float dpart[2][kRows];  // per-row partial sums of dO * O over each half of the columns
 };
 
-template <bool kBf16, int D, bool kDrop>
+template <bool kBf16, int D, int DV, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                  const __grid_constant__ CUtensorMap tm_dq, bwd::BwdParams p) {
-  using C = Config<D>;
+  using C = Config<D, DV>;
   using TQ = typename C::TQ;
+  using TG = typename C::TG;
   using TK = typename C::TK;
+  using TV = typename C::TV;
   constexpr int NSK = C::NSK;
   constexpr int NSV = C::NSV;
 
@@ -221,12 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && nsteps > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars.qg_full, 2 * TQ::kBytes);
+      mbar_arrive_expect_tx(&bars.qg_full, TQ::kBytes + TG::kBytes);
 #pragma unroll
-      for (int b = 0; b < TQ::L::kBoxes; ++b) {
+      for (int b = 0; b < TQ::L::kBoxes; ++b)
         tma_load_3d(sQ + b * TQ::kBoxBytes, &tm_q, &bars.qg_full, b * TQ::L::kBoxCols, row0, bh);
-        tma_load_3d(sG + b * TQ::kBoxBytes, &tm_g, &bars.qg_full, b * TQ::L::kBoxCols, row0, bh);
-      }
+#pragma unroll
+      for (int b = 0; b < TG::L::kBoxes; ++b)
+        tma_load_3d(sG + b * TG::kBoxBytes, &tm_g, &bars.qg_full, b * TG::L::kBoxCols, row0, bh);
       for (int i = 0; i < nsteps; ++i) {
         const int s = i % NSK;
         if (!mbar_wait_spin(&bars.k_empty[s], ((i / NSK) & 1) ^ 1, p.status, 42)) break;
@@ -238,10 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i + kPrefetch < nsteps) {
           const int kp = key0_at(i + kPrefetch);
 #pragma unroll
-          for (int b = 0; b < TK::L::kBoxes; ++b) {
-            tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, kp, bh);
-            tma_prefetch_l2_3d(&tm_v, b * TK::L::kBoxCols, kp, bh);
-          }
+          for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, kp, bh);
+#pragma unroll
+          for (int b = 0; b < TV::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_v, b * TV::L::kBoxCols, kp, bh);
         }
       }
     }
@@ -251,11 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < nsteps; ++i) {
         const int s = i % NSV;
         if (!mbar_wait_spin(&bars.v_empty[s], ((i / NSV) & 1) ^ 1, p.status, 41)) break;
-        mbar_arrive_expect_tx(&bars.v_full[s], TK::kBytes);
+        mbar_arrive_expect_tx(&bars.v_full[s], TV::kBytes);
 #pragma unroll
-        for (int b = 0; b < TK::L::kBoxes; ++b)
-          tma_load_3d(sV + s * TK::kBytes + b * TK::kBoxBytes, &tm_v, &bars.v_full[s],
-                      b * TK::L::kBoxCols, key0_at(i), bh);
+        for (int b = 0; b < TV::L::kBoxes; ++b)
+          tma_load_3d(sV + s * TV::kBytes + b * TV::kBoxBytes, &tm_v, &bars.v_full[s],
+                      b * TV::L::kBoxCols, key0_at(i), bh);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -266,8 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);  // S, dP
     constexpr uint32_t id_q = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dQ
     constexpr uint64_t kStage = TK::kBytes >> 4;
-    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TQ::desc_k(smem_u32(sG), 0);
-    const uint64_t dk0 = TK::desc_k(smem_u32(sK), 0), dv0 = TK::desc_k(smem_u32(sV), 0);
+    constexpr uint64_t kStageV = TV::kBytes >> 4;
+    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TG::desc_k(smem_u32(sG), 0);
+    const uint64_t dk0 = TK::desc_k(smem_u32(sK), 0), dv0 = TV::desc_k(smem_u32(sV), 0);
     const uint64_t dkmn0 = TK::desc_mn(smem_u32(sK), 0);
     bool ok = nsteps == 0 || mbar_wait_spin_warp(&bars.qg_full, 0, p.status, 43);
     auto issue_s = [&](int i) -> bool {
@@ -286,11 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_dp = [&](int i) -> bool {
       if (!mbar_wait_spin_warp(&bars.v_full[i % NSV], (i / NSV) & 1, p.status, 45)) return false;
       tc_fence_after();
-      const uint64_t dv = dv0 + static_cast<uint64_t>(i % NSV) * kStage;
+      const uint64_t dv = dv0 + static_cast<uint64_t>(i % NSV) * kStageV;
       if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP + (i & 1) * BN, dg0 + TQ::k_step(kk), dv + TK::k_step(kk), id_s,
+        for (int kk = 0; kk < DV / 16; ++kk)
+          mma_ss(tmem + C::kColDP + (i & 1) * BN, dg0 + TG::k_step(kk), dv + TV::k_step(kk), id_s,
                  kk > 0 ? 1u : 0u);
         mma_commit(&bars.dp_full[i & 1]);
         mma_commit(&bars.v_empty[i % NSV]);
@@ -338,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float dpar = 0.0f;
     if (row < n) {
       using E = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      const int64_t off = (static_cast<int64_t>(bh) * n + row) * D + half * (D / 2);
+      const int64_t off = (static_cast<int64_t>(bh) * n + row) * DV + half * (DV / 2);
       const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.o) + off);
       const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.d_o) + off);
 #pragma unroll
-      for (int v = 0; v < D / 16; ++v) {
+      for (int v = 0; v < DV / 16; ++v) {
         const uint4 a = __ldg(o4 + v), g = __ldg(g4 + v);
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll

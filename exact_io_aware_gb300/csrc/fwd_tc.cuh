@@ -14,7 +14,8 @@
 //              NSV stages); K runs one block ahead of V, and blocks kPrefetch steps ahead are
 //              requested into L2 so that the ring loads find them there
 // Tensor memory: S_t = Q_t K_jᵀ (BN fp32 columns per tile; the 16-bit P_t is written over
-// the first BN/2 of them) and O_t, the unnormalised weighted value sum z (D columns per tile).
+// the first BN/2 of them) and O_t, the unnormalised weighted value sum z (DV columns per tile,
+// DV the value width).
 // Each tile's MMA warp issues, per key block j, PV_{j-1} then S_j for its tile, so the tensor
 // core works on one tile while the other tile's softmax runs.  One issuer per tile keeps a
 // tile's waits (its softmax, the next K block) off the other tile's issue path: the tensor
@@ -66,19 +67,26 @@ constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 // Key blocks requested into L2 ahead of the ring loads.
 constexpr int kPrefetch = 4;
 
-template <int D, int BN>
+// D: width of Q and K rows; DV: width of V and O rows (the value width v, equal to D unless
+// the caller's values are wider or narrower than its keys).
+template <int D, int DV, int BN>
 struct Config {
   using TQ = Tile<kRowsPerTile, D>;
-  using TKV = Tile<BN, D>;
+  using TK = Tile<BN, D>;
+  using TV = Tile<BN, DV>;
+  using TO = Tile<kRowsPerTile, DV>;  // O staging, in the tile's Q slot
+  static constexpr int kQSlot = TQ::kBytes > TO::kBytes ? TQ::kBytes : TO::kBytes;
   static constexpr int kSmemBudget = kMaxDynSmem - 1024;  // minus the 1024-byte alignment slack
-  static constexpr int kFixed = 2 * TQ::kBytes;
+  static constexpr int kFixed = 2 * kQSlot;
   static constexpr int kStepReserve = 1024;  // smallest step table kept room for (bitmap masks)
-  static constexpr int kSlots = (kSmemBudget - kFixed - kStepReserve) / TKV::kBytes;
+  static constexpr int kAvail = kSmemBudget - kFixed - kStepReserve;
   // V is consumed one step after K, so K takes the odd slot: its loads are the ones a step waits on.
-  static constexpr int NSV = kSlots / 2 > 4 ? 4 : kSlots / 2;
-  static constexpr int NSK = kSlots - NSV > 4 ? 4 : kSlots - NSV;
+  static constexpr int kPairs = kAvail / (TK::kBytes + TV::kBytes);
+  static constexpr int NSV = kPairs > 4 ? 4 : kPairs;
+  static constexpr int kKFit = (kAvail - NSV * TV::kBytes) / TK::kBytes;
+  static constexpr int NSK = kKFit > 4 ? 4 : kKFit;
   static_assert(NSV >= 2 && NSK >= 2, "need at least two pipeline stages");
-  static constexpr int kTmemCols = 2 * BN + 2 * D;
+  static constexpr int kTmemCols = 2 * BN + 2 * DV;
   static constexpr int kTmemAlloc = kTmemCols <= 32    ? 32
                                     : kTmemCols <= 64  ? 64
                                     : kTmemCols <= 128 ? 128
@@ -87,9 +95,9 @@ struct Config {
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   // dynamic shared memory layout (offsets from a 1024-aligned base)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * TQ::kBytes;
-  static constexpr int kOffV = kOffK + NSK * TKV::kBytes;
-  static constexpr int kOffSteps = kOffV + NSV * TKV::kBytes;
+  static constexpr int kOffK = kOffQ + 2 * kQSlot;
+  static constexpr int kOffV = kOffK + NSK * TK::kBytes;
+  static constexpr int kOffSteps = kOffV + NSV * TV::kBytes;
   // Only a bitmap mask needs the step table (one word per key block); the walk under the
   // other masks is computed on the fly.
   static size_t smem_bytes(int n, int mask_kind) {
@@ -138,14 +146,16 @@ __device__ __forceinline__ uint32_t dense_step(int j, int BN, int nblk, int n, i
   return w;
 }
 
-template <bool kBf16, int D, int BN, bool kDrop>
+template <bool kBf16, int D, int DV, int BN, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   FwdParams p) {
-  using C = Config<D, BN>;
+  using C = Config<D, DV, BN>;
   using TQ = typename C::TQ;
-  using TKV = typename C::TKV;
+  using TK = typename C::TK;
+  using TV = typename C::TV;
+  using TO = typename C::TO;
   constexpr int NSK = C::NSK;
   constexpr int NSV = C::NSV;
 
@@ -274,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nsteps = bars.nsteps;
   const uint32_t tmem = bars.tmem_base;
   const uint32_t act = bars.act;
-  // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*D
+  // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*DV
   auto step_at = [&](int i) -> uint32_t {
     return use_table ? steps[i] : dense_step(j_lo + i, BN, nblk, n, nk, off, pair_row0, causal);
   };
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars.q_full[t], TQ::kBytes);
 #pragma unroll
         for (int b = 0; b < TQ::L::kBoxes; ++b)
-          tma_load_3d(sQ + t * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.q_full[t],
+          tma_load_3d(sQ + t * C::kQSlot + b * TQ::kBoxBytes, &tm_q, &bars.q_full[t],
                       b * TQ::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
       }
       // Ring loads in the order K_0, K_1, V_0, K_2, V_1, ...: K, which the next step waits
@@ -301,18 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % NSK;
         if (!mbar_wait(&bars.k_empty[s], ((i / NSK) & 1) ^ 1, p.status, 1)) return false;
         const int key0 = key0_at(i);
-        mbar_arrive_expect_tx(&bars.k_full[s], TKV::kBytes);
+        mbar_arrive_expect_tx(&bars.k_full[s], TK::kBytes);
 #pragma unroll
-        for (int b = 0; b < TKV::L::kBoxes; ++b)
-          tma_load_3d(sK + s * TKV::kBytes + b * TKV::kBoxBytes, &tm_k, &bars.k_full[s],
-                      b * TKV::L::kBoxCols, key0, bh);
+        for (int b = 0; b < TK::L::kBoxes; ++b)
+          tma_load_3d(sK + s * TK::kBytes + b * TK::kBoxBytes, &tm_k, &bars.k_full[s],
+                      b * TK::L::kBoxCols, key0, bh);
         if (i + kPrefetch < nsteps) {
           const int kp = key0_at(i + kPrefetch);
 #pragma unroll
-          for (int b = 0; b < TKV::L::kBoxes; ++b) {
-            tma_prefetch_l2_3d(&tm_k, b * TKV::L::kBoxCols, kp, bh);
-            tma_prefetch_l2_3d(&tm_v, b * TKV::L::kBoxCols, kp, bh);
-          }
+          for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, kp, bh);
+#pragma unroll
+          for (int b = 0; b < TV::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_v, b * TV::L::kBoxCols, kp, bh);
         }
         return true;
       };
@@ -320,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = i % NSV;
         if (!mbar_wait(&bars.v_empty[s], ((i / NSV) & 1) ^ 1, p.status, 2)) return false;
         const int key0 = key0_at(i);
-        mbar_arrive_expect_tx(&bars.v_full[s], TKV::kBytes);
+        mbar_arrive_expect_tx(&bars.v_full[s], TV::kBytes);
 #pragma unroll
-        for (int b = 0; b < TKV::L::kBoxes; ++b)
-          tma_load_3d(sV + s * TKV::kBytes + b * TKV::kBoxBytes, &tm_v, &bars.v_full[s],
-                      b * TKV::L::kBoxCols, key0, bh);
+        for (int b = 0; b < TV::L::kBoxes; ++b)
+          tma_load_3d(sV + s * TV::kBytes + b * TV::kBoxBytes, &tm_v, &bars.v_full[s],
+                      b * TV::L::kBoxCols, key0, bh);
         return true;
       };
       if (nsteps > 0 && load_k(0)) {
@@ -345,13 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 16-element step or a ring stage only adds a constant to the start-address field.
     const int t = warp;
     constexpr uint32_t id_s = idesc_f16(128, BN, kBf16 ? 1 : 0, 0, 0);
-    constexpr uint32_t id_o = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);
-    constexpr uint64_t kStage = TKV::kBytes >> 4;
-    const uint64_t dq = TQ::desc_k(smem_u32(sQ + t * TQ::kBytes), 0);
-    const uint64_t dk0 = TKV::desc_k(smem_u32(sK), 0);
-    const uint64_t dv0 = TKV::desc_mn(smem_u32(sV), 0);
+    constexpr uint32_t id_o = idesc_f16(128, DV, kBf16 ? 1 : 0, 0, 1);
+    constexpr uint64_t kStageK = TK::kBytes >> 4;
+    constexpr uint64_t kStageV = TV::kBytes >> 4;
+    const uint64_t dq = TQ::desc_k(smem_u32(sQ + t * C::kQSlot), 0);
+    const uint64_t dk0 = TK::desc_k(smem_u32(sK), 0);
+    const uint64_t dv0 = TV::desc_mn(smem_u32(sV), 0);
     const uint32_t tS = tmem + t * BN;
-    const uint32_t tO = tmem + 2 * BN + t * D;
+    const uint32_t tO = tmem + 2 * BN + t * DV;
     bool ok = (act >> t) & 1u;
     if (ok) ok = mbar_wait_warp(&bars.q_full[t], 0, p.status, 3);
     bool pend = false;     // this tile took part in the previous step (PV owed)
@@ -375,21 +385,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         pph ^= 1u;
         tc_fence_after();
-        const uint64_t dv = dv0 + static_cast<uint64_t>(prev % NSV) * kStage;
+        const uint64_t dv = dv0 + static_cast<uint64_t>(prev % NSV) * kStageV;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tO, tS + kk * 8, dv + TKV::mn_step(kk), id_o, (started || kk > 0) ? 1u : 0u);
+            mma_ts(tO, tS + kk * 8, dv + TV::mn_step(kk), id_o, (started || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
         started = true;
       }
       if (cur) {
-        const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kStage;
+        const uint64_t dk = dk0 + static_cast<uint64_t>(s) * kStageK;
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tS, dq + TQ::k_step(kk), dk + TKV::k_step(kk), id_s, kk > 0 ? 1u : 0u);
+            mma_ss(tS, dq + TQ::k_step(kk), dk + TK::k_step(kk), id_s, kk > 0 ? 1u : 0u);
           mma_commit(&bars.s_full[t]);
         }
         __syncwarp();
@@ -410,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;
     const int row = pair_row0 + t * kRowsPerTile + r;
     const uint32_t tS = tmem + t * BN;
-    const uint32_t tO = tmem + 2 * BN + t * D;
+    const uint32_t tO = tmem + 2 * BN + t * DV;
     const bool active = (act >> t) & 1u;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     // The scale c·log2(e) is folded into the exponent's FFMA, so the raw scores are reduced:
@@ -528,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (rare with the lazy threshold, so the loop stays rolled and out of the common path).
       if (__builtin_expect(!first && __any_sync(0xFFFFFFFFu, alpha != 1.0f), 0)) {
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = 0; c0 < DV; c0 += 16) {
           uint32_t rr[16];
           tmem_ld16(tO + lane_off + c0, rr);
           tmem_wait_ld();
@@ -582,9 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // only the stores are per row.
         if (ok) {
           const int64_t prow = (static_cast<int64_t>(split) * gridDim.y + bh) * n + row;
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * DV);
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 16) {
+          for (int c0 = 0; c0 < DV; c0 += 16) {
             uint32_t rr[16];
             if (active) {
               tmem_ld16(tO + lane_off + c0, rr);
@@ -611,10 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
       tc_fence_after();
       const float inv = l > 0.0f ? (kDrop ? p.drop.scale : 1.0f) / l : 0.0f;
-      uint8_t* stage = sQ + t * TQ::kBytes;  // Q_t is dead once every MMA of tile t is done
+      uint8_t* stage = sQ + t * C::kQSlot;  // Q_t is dead once every MMA of tile t is done
       if (ok) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = 0; c0 < DV; c0 += 16) {
           uint32_t rr[16];
           if (active) {
             tmem_ld16(tO + lane_off + c0, rr);
@@ -628,9 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k)
             pk[k] = pack2<kBf16>(__uint_as_float(rr[2 * k]) * inv,
                                  __uint_as_float(rr[2 * k + 1]) * inv);
-          *reinterpret_cast<uint4*>(stage + TQ::offset(r, c0)) =
+          *reinterpret_cast<uint4*>(stage + TO::offset(r, c0)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(stage + TQ::offset(r, c0 + 8)) =
+          *reinterpret_cast<uint4*>(stage + TO::offset(r, c0 + 8)) =
               make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
         if (row < n) {
@@ -643,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_barrier(1 + t, 128);
       if (ok && r == 0) {
 #pragma unroll
-        for (int b = 0; b < TQ::L::kBoxes; ++b)
-          tma_store_3d(&tm_o, stage + b * TQ::kBoxBytes, b * TQ::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
+        for (int b = 0; b < TO::L::kBoxes; ++b)
+          tma_store_3d(&tm_o, stage + b * TO::kBoxBytes, b * TO::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
         tma_store_commit();
         tma_store_wait_all();
       }

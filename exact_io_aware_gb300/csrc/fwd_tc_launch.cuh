@@ -9,9 +9,9 @@
 namespace ea {
 namespace fwd {
 
-template <bool kBf16, int D, int BN, bool kDrop>
+template <bool kBf16, int D, int DV, int BN, bool kDrop>
 int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
-  using Cfg = Config<D, BN>;
+  using Cfg = Config<D, DV, BN>;
   const int nk = a.nk > 0 ? a.nk : a.n;
   const size_t smem = Cfg::smem_bytes(nk, a.mask_kind);
   if (smem > static_cast<size_t>(kMaxDynSmem)) {
@@ -22,14 +22,15 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;
   CUtensorMap tq, tk, tv, to;
   constexpr uint32_t bc = RowLayout<D>::kBoxCols;
+  constexpr uint32_t bcv = RowLayout<DV>::kBoxCols;
   if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, kRowsPerTile, bc) ||
       !encode_tile_map(&tk, a.k, kBf16, heads, nk, D, BN, bc) ||
-      !encode_tile_map(&tv, a.v, kBf16, heads, nk, D, BN, bc) ||
-      !encode_tile_map(&to, a.o_out, kBf16, heads, a.n, D, kRowsPerTile, bc)) {
+      !encode_tile_map(&tv, a.v, kBf16, heads, nk, DV, BN, bcv) ||
+      !encode_tile_map(&to, a.o_out, kBf16, heads, a.n, DV, kRowsPerTile, bcv)) {
     err = "cuTensorMapEncodeTiled rejected a forward tensor map";
     return -5;
   }
-  auto kern = fwd_tc_kernel<kBf16, D, BN, kDrop>;
+  auto kern = fwd_tc_kernel<kBf16, D, DV, BN, kDrop>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
@@ -51,21 +52,24 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   return 0;
 }
 
-template <int D, bool kDrop>
+template <int D, int DV, bool kDrop>
 int launch_dd(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
   const int bn = a.kv_block == 0 ? 128 : a.kv_block;
   switch (bn) {
-    case 32: return bf16 ? run<true, D, 32, kDrop>(a, s, err) : run<false, D, 32, kDrop>(a, s, err);
-    case 64: return bf16 ? run<true, D, 64, kDrop>(a, s, err) : run<false, D, 64, kDrop>(a, s, err);
+    case 32:
+      return bf16 ? run<true, D, DV, 32, kDrop>(a, s, err) : run<false, D, DV, 32, kDrop>(a, s, err);
+    case 64:
+      return bf16 ? run<true, D, DV, 64, kDrop>(a, s, err) : run<false, D, DV, 64, kDrop>(a, s, err);
     case 128:
-      return bf16 ? run<true, D, 128, kDrop>(a, s, err) : run<false, D, 128, kDrop>(a, s, err);
+      return bf16 ? run<true, D, DV, 128, kDrop>(a, s, err) : run<false, D, DV, 128, kDrop>(a, s, err);
     default: err = "kv_block must be 0, 32, 64 or 128"; return -2;
   }
 }
 
-template <int D>
+// Instantiations with and without dropout for one (key width, value width) pair.
+template <int D, int DV = D>
 int launch_d(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
-  return a.dropout ? launch_dd<D, true>(bf16, a, s, err) : launch_dd<D, false>(bf16, a, s, err);
+  return a.dropout ? launch_dd<D, DV, true>(bf16, a, s, err) : launch_dd<D, DV, false>(bf16, a, s, err);
 }
 
 }  // namespace fwd

@@ -36,6 +36,7 @@ struct FwdParams {
 // Everything a launcher needs; pointers are device pointers.
 struct AttnArgs {
   int B, H, n, d;
+  int v_dim;  // value width (columns of V, O, dO, dV); d unless the values are wider or narrower
   int nk;  // keys; the forward allows nk != n (queries at the end of the key sequence)
   float c;
   const void* q;

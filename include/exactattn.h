@@ -293,6 +293,33 @@ int attn_bwd_dropout(int dtype, int B, int H, int n, int d, float c,
                      void* stream);
 
 /*
+ * Forward and backward with values of their own width v (v_dim): Q, K in R^{n x d} and V in
+ * R^{n x v}, the general shape of "Exact tiled attention and memory-aware differentiation"
+ * (inputs n, d, v; output Y in R^{n x v}).  Scores and their gradients live in the d-wide
+ * space, O, dO and dV in the v-wide one:
+ *   q, k, dq, dk   [B][H][n][d]
+ *   v, o, d_o, dv  [B][H][n][v_dim]
+ * Supported: v_dim = d (the same as attn_fwd_dropout / attn_bwd_dropout), or (d, v_dim) =
+ * (64, 128) or (128, 64), in every dtype, with every mask, key block and dropout (p_drop = 0:
+ * none; the mask and seed rules of attn_fwd_dropout).  The backward's workspace is
+ * attn_bwd_workspace_bytes(dtype, B, H, n, d).  Other arguments, outputs and errors as for
+ * attn_fwd_dropout and attn_bwd_dropout; ATTN_ERR_UNSUPPORTED for another (d, v_dim) pair.
+ */
+int attn_fwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c,
+                  const void* q, const void* k, const void* v,
+                  int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                  int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed,
+                  void* o, float* lse, void* stream);
+
+int attn_bwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c,
+                  const void* q, const void* k, const void* v, const void* o,
+                  const float* lse, const void* d_o,
+                  int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
+                  int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/*
  * attn_bwd without a workspace argument, for callers that cannot allocate device memory at
  * the time they call the backward: an engine or framework that owns every device allocation
  * and gives its plugins no allocator, or a system that fixes its memory budget at start-up

@@ -182,10 +182,13 @@ def test_tiled_forward_equals_dense_for_every_block_size(kind):
         assert np.max(np.abs(tm + np.log(tl) - lse)) <= 1e-12
 
 
-def test_reverse_procedure_equals_dense_backward():
+@pytest.mark.parametrize("vw", [4, 7, 2])
+def test_reverse_procedure_equals_dense_backward(vw):
+    """Value width vw = d and vw != d (the general shape: V and G have their own width)."""
     rng = _rng(22)
     n, d = 23, 4
-    q, k, val, g = (rng.normal(size=(n, d)) for _ in range(4))
+    q, k = (rng.normal(size=(n, d)) for _ in range(2))
+    val, g = (rng.normal(size=(n, vw)) for _ in range(2))
     c = 0.9
     a = _random_allowed(rng, n)
     dq, dk, dv, y, lse = attention.backward_head(q, k, val, c, a, g)
@@ -201,11 +204,12 @@ def _phi(q, k, v, c, a, g):
     return float((g * y).sum())
 
 
-@pytest.mark.parametrize("tied", [False, True])
-def test_gradient_matches_central_differences(tied):
+@pytest.mark.parametrize("tied,vw", [(False, 3), (True, 3), (False, 5), (False, 2)])
+def test_gradient_matches_central_differences(tied, vw):
     rng = _rng(23 + tied)
     n, d = 7, 3
-    q, k, v, g = (rng.normal(size=(n, d)) for _ in range(4))
+    q, k = (rng.normal(size=(n, d)) for _ in range(2))
+    v, g = (rng.normal(size=(n, vw)) for _ in range(2))
     c = 0.8
     a = _random_allowed(rng, n, 0.6)
     a[2, :] = True
