@@ -50,6 +50,7 @@ def main(argv=None):
                     help="with --fp8: attn_fp8_quantize (timed apart) + attn_fwd_fp8_blocks")
     ap.add_argument("--rotate", action="store_true",
                     help="with --fp8-blocks: incoherent processing of Q and K")
+    ap.add_argument("--vdim", type=int, default=0, help="value width v (default: d)")
     ap.add_argument("--json", action="store_true", help="print one JSON line")
     a = ap.parse_args(argv)
 
@@ -80,10 +81,12 @@ def main(argv=None):
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
     shape = (B, H, n, d)
-    q, k, v, do = (torch.randn(shape, device="cuda", generator=g) for _ in range(4))
+    vd = a.vdim or d
+    q, k = (torch.randn(shape, device="cuda", generator=g) for _ in range(2))
+    v, do = (torch.randn((B, H, n, vd), device="cuda", generator=g) for _ in range(2))
     q = (q * qs).to(dt)
     k, v, do = k.to(dt), v.to(dt), do.to(dt)
-    o = torch.empty_like(q)
+    o = torch.empty_like(v)
     lse = torch.empty(shape[:3], device="cuda", dtype=torch.float32)
     ws = torch.empty(ea.attn_bwd_workspace_bytes(dt, *shape), dtype=torch.uint8, device="cuda")
     splits, fws = 1, None
@@ -109,12 +112,14 @@ def main(argv=None):
     status = ea.attn_device_status()
     fwd_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev[1:]]))
     bwd_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev[1:]])) if not fwd_only else None
-    fl = 4.0 * B * H * n * n * d * kappa
-    out = {"workload": name, "B": B, "H": H, "n": n, "d": d, "dtype": dtype, "mask": mask,
+    # forward: S (width d) and P V (width v); backward: S, dK, dQ (d) and dP, dV (v)
+    fl = 2.0 * B * H * n * n * (d + vd) * kappa
+    fl_b = 2.0 * B * H * n * n * (3 * d + 2 * vd) * kappa
+    out = {"workload": name, "B": B, "H": H, "n": n, "d": d, "v": vd, "dtype": dtype, "mask": mask,
            "kv_block": kvb, "splits": splits, "dropout": a.dropout, "kappa": kappa, "fwd_ms": fwd_ms,
            "fwd_tflops": fl / (fwd_ms / 1e3) / 1e12, "status": status}
     if bwd_ms is not None:
-        out.update(bwd_ms=bwd_ms, bwd_tflops=2.5 * fl / (bwd_ms / 1e3) / 1e12)
+        out.update(bwd_ms=bwd_ms, bwd_tflops=fl_b / (bwd_ms / 1e3) / 1e12)
     if a.json:
         print(json.dumps(out))
     else:
