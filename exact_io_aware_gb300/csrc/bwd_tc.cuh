@@ -62,10 +62,11 @@ struct BwdParams {
   float* L2;
   float* Dv;
   int n_pad;
-  // inputs the dQ kernel builds the table from
+  // inputs the dQ kernel builds the table from (and the rows it loads into tensor memory)
   const float* lse;
   const void* o;
   const void* d_o;
+  const void* q;
   uint32_t* status;
   DropoutArgs drop;  // read only by the dropout instantiations
 };

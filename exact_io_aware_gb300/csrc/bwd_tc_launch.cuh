@@ -38,7 +38,8 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   const int n_pad = bwd_pad_rows(a.n);
   float* L2 = table;
   BwdParams p{a.n,  a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
-              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.status};
+              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.q,
+              a.status};
   p.drop = a.drop;
   const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
   // the dQ kernel writes the row table the dK/dV kernel reads
@@ -46,7 +47,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   cudaError_t e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(qsmem));
   if (e == cudaSuccess) {
-    qkern<<<grid, dq::kThreads, qsmem, s>>>(tq, tk, tv, tg, tdq, p);
+    qkern<<<grid, dq::kThreads, qsmem, s>>>(tk, tv, tdq, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

@@ -11,28 +11,34 @@
 // kernel computes D_i = rowsum(dO_i * O_i) itself (each softmax warp of a row sums half of
 // the columns) and writes the row table (LSE_i log2 e and D_i) that the dK/dV kernel, launched
 // after it, copies per query block.
-// Per key block j:
-//   S  = Q K_jᵀ           (tensor memory, one query row per lane; one buffer, free again as
-//                          soon as the softmax warps have loaded it)
+// Q and dO are the same for every key block, so the softmax warps write them into tensor
+// memory once (the rows they load for D_i anyway; 16-bit pairs per column, the A-operand
+// layout), and all three products read only their B operand from shared memory.  With both
+// operands in shared memory a 128 x 128 x 16 product needs the SM's whole shared-memory
+// bandwidth, and the products ran at ~88 instead of ~64 cycles.  Per key block j:
+//   S  = Q K_jᵀ           (A = Q in tensor memory; one buffer, free again as soon as the
+//                          softmax warps have loaded it)
 //   P  = exp2(S c log2e - LSE log2e)     softmax warps, kept in registers
-//   dP = dO V_jᵀ          (two buffers, so dP_{j+1} is computed while dQ_j reads dS_j)
+//   dP = dO V_jᵀ          (A = dO in tensor memory; one buffer)
 //   dS = P (dP - D)                      softmax warps; 16-bit, written over dP
-//   dQ += dS K_j                         (A operand read from tensor memory)
+//   dQ += dS K_j                         (A = dS in tensor memory)
 // Dropout (kDrop): dS = P (keep ? dP/(1-p) : 0) - P D with the mask of dropout.cuh redrawn for
 // the block's (query, key) pairs; P itself is not masked here (dQ needs only dS).
 // Roles (the control warps take the lowest warp slots, which the warp schedulers favour over
 // the softmax warps they share a sub-partition with):
 //   warp  0    TMEM allocator and MMA issuer
-//   warp  1    TMA producer of Q, dO (once) and the K ring (NSK stages); blocks a few steps
-//              ahead are requested into L2
+//   warp  1    TMA producer of the K ring (NSK stages); blocks a few steps ahead are
+//              requested into L2
 //   warp  2    TMA producer of the V ring (NSV stages): the two rings are released by
 //              different products (K after dQ, V after dP), so neither waits on the other
 //   warps 3-10 softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 3) / 4 of the
-//              block's key columns; warps 3-6 also write dQ at the end
-// Issue order per block i: [S_{i+1} once S_i is loaded], [dP_{i+1}], dQ_i.  dP_{i+1} goes to the
-// buffer that dQ_{i-1}, issued before it, read; so the softmax warps find dP_{i+1} ready when
-// they finish dS_i, and the tensor core runs dQ_i while they work on block i+1.  K is held
-// from S_i to dQ_i, across two issue rounds, hence its deeper ring.
+//              block's key columns (and of Q's and dO's columns when it loads them); warps
+//              3-6 also write dQ at the end
+// Issue order per block i: [S_{i+1} once S_i is loaded], dQ_i once dS_i is written, then
+// dP_{i+1}, which overwrites dS_i after dQ_i has read it (one thread's MMAs run in issue
+// order).  The softmax warps compute P_{i+1} while dQ_i and dP_{i+1} run, and the tensor core
+// runs S_{i+2} while they compute dS_{i+1}.  K is held from S_i to dQ_i, across two issue
+// rounds, hence its deeper ring.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -63,19 +69,20 @@ using bwd::unpack2;
 // D: width of Q, K, dQ rows; DV: width of V, dO rows (the value width).
 template <int D, int DV>
 struct Config {
-  using TQ = Tile<kRows, D>;   // Q (and dQ staging)
-  using TG = Tile<kRows, DV>;  // dO
+  using TQ = Tile<kRows, D>;   // dQ staging
   using TK = Tile<BN, D>;      // K stages
   using TV = Tile<BN, DV>;     // V stages
-  // tensor-memory columns: S, dP buffers, dQ
+  // tensor-memory columns: S, dP, dQ, then Q and dO (two 16-bit elements a column)
   static constexpr int kColS = 0;
-  static constexpr int kColDP = BN;  // buffer b at BN + b * BN
-  static constexpr int kColDQ = 3 * BN;
-  static constexpr int kTmemCols = kColDQ + pad32(D);
+  static constexpr int kColDP = BN;
+  static constexpr int kColDQ = 2 * BN;
+  static constexpr int kColQ = kColDQ + pad32(D);
+  static constexpr int kColG = kColQ + pad32(D / 2);
+  static constexpr int kTmemCols = kColG + DV / 2;
   static_assert(kTmemCols <= 512, "tensor memory overflow");
   static constexpr int kTmemAlloc = 512;
   static constexpr int kBudget = 227 * 1024 - 2048;  // dynamic limit less alignment slack
-  static constexpr int kFixed = TQ::kBytes + TG::kBytes;
+  static constexpr int kFixed = TQ::kBytes;
   static constexpr int kStepReserve = 1024;  // smallest step table kept room for (bitmap masks)
   static constexpr int kAvail = kBudget - kFixed - kStepReserve;
   static constexpr int kPairs = kAvail / (TK::kBytes + TV::kBytes);
@@ -84,8 +91,7 @@ struct Config {
   static constexpr int NSK = kKFit > 4 ? 4 : kKFit;
   static_assert(NSV >= 2 && NSK >= 2, "need two key and two value stages");
   static constexpr int kOffQ = 0;
-  static constexpr int kOffG = kOffQ + TQ::kBytes;
-  static constexpr int kOffK = kOffG + TG::kBytes;
+  static constexpr int kOffK = kOffQ + TQ::kBytes;
   static constexpr int kOffV = kOffK + NSK * TK::kBytes;
   static constexpr int kOffSteps = kOffV + NSV * TV::kBytes;
   // Only a bitmap mask needs the step table; the walk under the other masks is computed.
@@ -95,23 +101,37 @@ struct Config {
 };
 
 struct Barriers {
-  uint64_t qg_full;
+  uint64_t qg_full;  // Q and dO are in tensor memory (one arrival per softmax warp)
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full, s_free, dp_full[2], ds_full;
+  uint64_t s_full, s_free, dp_full, ds_full;
   uint64_t dq_done;
   uint32_t tmem_base;
   uint32_t nsteps;
   float dpart[2][kRows];  // per-row partial sums of dO * O over each half of the columns
 };
 
+// Stores n consecutive 32-bit columns of this thread's TMEM lane (n = 4, 8, 16 or 32).
+template <int N>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&w)[N]) {
+  if constexpr (N == 4) {
+    tmem_st4(taddr, w);
+  } else if constexpr (N == 8) {
+    tmem_st8(taddr, w);
+  } else if constexpr (N == 16) {
+    tmem_st16(taddr, w);
+  } else {
+    static_assert(N == 32, "4, 8, 16 or 32 columns");
+    tmem_st16(taddr, *reinterpret_cast<const uint32_t(*)[16]>(&w[0]));
+    tmem_st16(taddr + 16, *reinterpret_cast<const uint32_t(*)[16]>(&w[16]));
+  }
+}
+
 template <bool kBf16, int D, int DV, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
-    dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_dq, bwd::BwdParams p) {
   using C = Config<D, DV>;
   using TQ = typename C::TQ;
-  using TG = typename C::TG;
   using TK = typename C::TK;
   using TV = typename C::TV;
   constexpr int NSK = C::NSK;
@@ -120,7 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = bwd::align1024(smem_raw);
   uint8_t* sQ = smem + C::kOffQ;
-  uint8_t* sG = smem + C::kOffG;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint32_t* steps = reinterpret_cast<uint32_t*>(smem + C::kOffSteps);
@@ -137,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
-    mbar_init(&bars.qg_full, 1);
+    mbar_init(&bars.qg_full, kSoftmaxWarps);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -148,8 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars.s_full, 1);
     mbar_init(&bars.s_free, kSoftmaxWarps);
-    mbar_init(&bars.dp_full[0], 1);
-    mbar_init(&bars.dp_full[1], 1);
+    mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_full, kSoftmaxWarps);
     mbar_init(&bars.dq_done, 1);
     fence_barrier_init();
@@ -224,17 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto key0_at = [&](int i) { return static_cast<int>(step_at(i) & 0xFFFFu) * BN; };
   if (warp == kKProducerWarp) {
-    // ---------------------------------------------------------------- TMA producer: Q, dO, K
+    // ---------------------------------------------------------------- TMA producer: K
     if (lane == 0 && nsteps > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      mbar_arrive_expect_tx(&bars.qg_full, TQ::kBytes + TG::kBytes);
-#pragma unroll
-      for (int b = 0; b < TQ::L::kBoxes; ++b)
-        tma_load_3d(sQ + b * TQ::kBoxBytes, &tm_q, &bars.qg_full, b * TQ::L::kBoxCols, row0, bh);
-#pragma unroll
-      for (int b = 0; b < TG::L::kBoxes; ++b)
-        tma_load_3d(sG + b * TG::kBoxBytes, &tm_g, &bars.qg_full, b * TG::L::kBoxCols, row0, bh);
       for (int i = 0; i < nsteps; ++i) {
         const int s = i % NSK;
         if (!mbar_wait_spin(&bars.k_empty[s], ((i / NSK) & 1) ^ 1, p.status, 42)) break;
@@ -274,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_q = idesc_f16(128, D, kBf16 ? 1 : 0, 0, 1);   // dQ
     constexpr uint64_t kStage = TK::kBytes >> 4;
     constexpr uint64_t kStageV = TV::kBytes >> 4;
-    const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TG::desc_k(smem_u32(sG), 0);
     const uint64_t dk0 = TK::desc_k(smem_u32(sK), 0), dv0 = TV::desc_k(smem_u32(sV), 0);
     const uint64_t dkmn0 = TK::desc_mn(smem_u32(sK), 0);
     bool ok = nsteps == 0 || mbar_wait_spin_warp(&bars.qg_full, 0, p.status, 43);
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS, dq0 + TQ::k_step(kk), dk + TK::k_step(kk), id_s, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8, dk + TK::k_step(kk), id_s, kk > 0 ? 1u : 0u);
         mma_commit(&bars.s_full);
       }
       __syncwarp();
@@ -298,9 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
-          mma_ss(tmem + C::kColDP + (i & 1) * BN, dg0 + TG::k_step(kk), dv + TV::k_step(kk), id_s,
+          mma_ts(tmem + C::kColDP, tmem + C::kColG + kk * 8, dv + TV::k_step(kk), id_s,
                  kk > 0 ? 1u : 0u);
-        mma_commit(&bars.dp_full[i & 1]);
+        mma_commit(&bars.dp_full);
         mma_commit(&bars.v_empty[i % NSV]);
       }
       __syncwarp();
@@ -313,22 +323,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_spin_warp(&bars.s_free, i & 1, p.status, 50);
         if (!ok) break;
         tc_fence_after();
-        ok = issue_s(i + 1) && issue_dp(i + 1);
+        ok = issue_s(i + 1);
         if (!ok) break;
       }
       ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 46);
       if (!ok) break;
       tc_fence_after();
       const uint64_t dkmn = dkmn0 + static_cast<uint64_t>(i % NSK) * kStage;
-      const uint32_t ds_col = C::kColDP + (i & 1) * BN;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + C::kColDQ, tmem + ds_col + packed_col(16 * kk), dkmn + TK::mn_step(kk),
+          mma_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(16 * kk), dkmn + TK::mn_step(kk),
                  id_q, (i > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars.k_empty[i % NSK]);
       }
       __syncwarp();
+      // dP_{i+1} overwrites dS_i, which dQ_i (issued before it) has read
+      if (i + 1 < nsteps) {
+        ok = issue_dp(i + 1);
+        if (!ok) break;
+      }
     }
     if (elect_one()) mma_commit(&bars.dq_done);
     __syncwarp();
@@ -342,16 +356,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - kFirstSoftmaxWarp) / 4;
     const int c_lo = half * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
-    // D_i: this warp sums dO * O over its half of the head dimension (16-byte loads)
+    // D_i: this warp sums dO * O over its half of the value columns (16-byte loads).  The
+    // same dO words, and this half of the row's Q, go into tensor memory as the A operands of
+    // dP and S: memory order puts element 2c in the low half of word c, which is the operand
+    // layout (two 16-bit elements a column).  Rows past n get zeros.
     float dpar = 0.0f;
-    if (row < n) {
+    {
       using E = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
-      const int64_t off = (static_cast<int64_t>(bh) * n + row) * DV + half * (DV / 2);
-      const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.o) + off);
-      const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.d_o) + off);
+      constexpr int kGW = DV / 4;  // dO columns of this half
+      constexpr int kQW = D / 4;   // Q columns of this half
+      uint32_t gcol[kGW], qcol[kQW];
+      const bool in = row < n;
+      const int64_t rr = static_cast<int64_t>(bh) * n + (in ? row : 0);
+      const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.o) + rr * DV + half * (DV / 2));
+      const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.d_o) + rr * DV + half * (DV / 2));
+      const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + rr * D + half * (D / 2));
 #pragma unroll
       for (int v = 0; v < DV / 16; ++v) {
-        const uint4 a = __ldg(o4 + v), g = __ldg(g4 + v);
+        const uint4 a = in ? __ldg(o4 + v) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 g = in ? __ldg(g4 + v) : make_uint4(0u, 0u, 0u, 0u);
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -360,8 +383,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           unpack2<kBf16>(gw[e], g0, g1);
           dpar = fmaf(a0, g0, dpar);
           dpar = fmaf(a1, g1, dpar);
+          gcol[4 * v + e] = gw[e];
         }
       }
+#pragma unroll
+      for (int v = 0; v < D / 16; ++v) {
+        const uint4 q = in ? __ldg(q4 + v) : make_uint4(0u, 0u, 0u, 0u);
+        qcol[4 * v] = q.x;
+        qcol[4 * v + 1] = q.y;
+        qcol[4 * v + 2] = q.z;
+        qcol[4 * v + 3] = q.w;
+      }
+      st_cols<kQW>(tmem + lane_off + C::kColQ + half * kQW, qcol);
+      st_cols<kGW>(tmem + lane_off + C::kColG + half * kGW, gcol);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.qg_full);
     }
     bars.dpart[half][r] = dpar;
     bwd::named_barrier(3, kSoftmaxWarps * 32);
@@ -401,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tS = tmem + C::kColS + lane_off;
-      const uint32_t tP = tmem + C::kColDP + (i & 1) * BN + lane_off;
+      const uint32_t tP = tmem + C::kColDP + lane_off;
       uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
       // both 32-column chunks are loaded before one wait: the load latency is paid once
       uint32_t rr[kHalf / 32][32];
@@ -450,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           kbits[h] = w;
         }
       }
-      ok = mbar_wait_spin(&bars.dp_full[i & 1], (i >> 1) & 1, p.status, 48);
+      ok = mbar_wait_spin(&bars.dp_full, i & 1, p.status, 48);
       if (!ok) break;
       tc_fence_after();
       uint32_t dp[kHalf / 32][32];
