@@ -11,8 +11,8 @@
 //   warps 2-5  softmax for tile 0   (thread = query row = TMEM lane of the warp's quadrant)
 //   warps 6-9  softmax for tile 1
 //   warp  10   TMA producer: Q tiles once, then K and V blocks through two rings (NSK and
-//              NSV stages); K runs one block ahead of V, and blocks kPrefetch steps ahead are
-//              requested into L2 so that the ring loads find them there
+//              NSV stages); K runs one block ahead of V, and (full query tiles only) blocks
+//              kPrefetch steps ahead are requested into L2 so that the ring loads find them
 // Tensor memory: S_t = Q_t K_jᵀ (BN fp32 columns per tile; the 16-bit P_t is written over
 // the first BN/2 of them) and O_t, the unnormalised weighted value sum z (DV columns per tile,
 // DV the value width).
@@ -64,7 +64,11 @@ constexpr uint32_t kSkip = 0, kFull = 1, kPartial = 2;
 // Opt-in dynamic shared memory per CTA on sm_103a (227 KiB) less the kernel's static barrier
 // block.
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;
-// Key blocks requested into L2 ahead of the ring loads.
+// Key blocks requested into L2 ahead of the ring loads when the CTA's query tiles are full
+// (compute-bound).  With a few query rows (decoding over a key/value cache) the CTA streams
+// K and V at the HBM rate, and the early requests cost re-reads from DRAM (measured: reads
+// 1.235x the K/V bytes with them, 1.000x without, and 22 % less time), so the launcher sets
+// the distance to 0 there.
 constexpr int kPrefetch = 4;
 
 // D: width of Q and K rows; DV: width of V and O rows (the value width v, equal to D unless
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < TK::L::kBoxes; ++b)
           tma_load_3d(sK + s * TK::kBytes + b * TK::kBoxBytes, &tm_k, &bars.k_full[s],
                       b * TK::L::kBoxCols, key0, bh);
-        if (i + kPrefetch < nsteps) {
-          const int kp = key0_at(i + kPrefetch);
+        if (p.prefetch > 0 && i + p.prefetch < nsteps) {
+          const int kp = key0_at(i + p.prefetch);
 #pragma unroll
           for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, kp, bh);
 #pragma unroll

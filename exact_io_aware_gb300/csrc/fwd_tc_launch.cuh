@@ -40,7 +40,8 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   const int nsplit = a.num_splits > 1 ? a.num_splits : 1;
   FwdParams p{a.n, a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
               a.lse, a.status, nsplit, nsplit > 1 ? a.o_part : nullptr,
-              nsplit > 1 ? a.lse_part : nullptr, a.drop, nk, nk - a.n};
+              nsplit > 1 ? a.lse_part : nullptr, a.drop, nk, nk - a.n,
+              a.n >= kRowsPerTile ? kPrefetch : 0};
   dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads),
             static_cast<unsigned>(nsplit));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);

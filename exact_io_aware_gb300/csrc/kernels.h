@@ -31,6 +31,7 @@ struct FwdParams {
   DropoutArgs drop;  // read only by the dropout instantiations
   int nk;            // keys (n for square attention)
   int off;           // causal offset nk - n: query i sees keys j <= i + off
+  int prefetch;      // key blocks requested into L2 ahead of the ring loads (0: none)
 };
 
 // Everything a launcher needs; pointers are device pointers.
