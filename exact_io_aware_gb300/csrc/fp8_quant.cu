@@ -78,7 +78,7 @@ __device__ __forceinline__ float block_max(float v, float* red) {
 }
 
 template <bool kBf16, int D>
-__global__ void __launch_bounds__(kThreads) quant_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads, 3) quant_kernel(Params p) {
   __shared__ float red[kThreads / 32];
   const int blk = blockIdx.x;
   const int bh = blockIdx.y;
