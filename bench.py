@@ -20,6 +20,7 @@ import argparse
 import json
 import os
 import statistics
+import select
 import subprocess
 import sys
 import time
@@ -104,6 +105,12 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            # nvidia-smi takes a while to start: wait (at most 5 s) for its first sample, taken
+            # before the timed region and dropped, so that the region is sampled from its start
+            ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+            if ready:
+                self.proc.stdout.readline()
         return self
 
     def __exit__(self, *exc):

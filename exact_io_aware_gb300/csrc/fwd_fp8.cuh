@@ -332,18 +332,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool pos = sl2 > 0.0f;
     const float mv = pos ? -INFINITY : INFINITY;
     constexpr bool blocks = kBlocks;
-    const int64_t sbase = static_cast<int64_t>(bh) * nblk;
-    float kq = sl2;      // score factor without the key block's scale
-    float vmax = p.sv;   // value scale of the epilogue
-    float l2vmax = 0.0f;
-    if (blocks) {
-      kq = sl2 * __ldg(p.sq_blk + sbase + min(pair * 2 + t, nblk - 1));
+    const int sbase = bh * nblk;  // this head's first block scale
+    // largest value-block scale of the head (every lane gets it)
+    auto head_vmax = [&]() -> float {
       float mxv = 0.0f;
       for (int jb = lane; jb < nblk; jb += 32) mxv = fmaxf(mxv, __ldg(p.sv_blk + sbase + jb));
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mxv = fmaxf(mxv, __shfl_xor_sync(0xFFFFFFFFu, mxv, o));
-      vmax = mxv;
-      l2vmax = __log2f(mxv);
+      return mxv;
+    };
+    float kq = sl2;  // score factor without the key block's scale
+    float l2vmax = 0.0f;
+    if (blocks) {
+      kq = sl2 * __ldg(p.sq_blk + sbase + min(pair * 2 + t, nblk - 1));
+      l2vmax = __log2f(head_vmax());
     }
     float m = -INFINITY;  // exact running maximum, log2 units
     float l = 0.0f;       // running sum of 2^8 exp(score - m)
@@ -478,6 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pair_row0 + t * kRowsPerTile < n) {
       if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
       tc_fence_after();
+      const float vmax = blocks ? head_vmax() : p.sv;  // reloaded: not held through the loop
       const float inv = l > 0.0f ? vmax / l : 0.0f;
       if (ok) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + (static_cast<int64_t>(bh) * n + row) * D);
