@@ -132,7 +132,7 @@ def _e4m3_step(c):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("n", [128, 336])
+@pytest.mark.parametrize("n", [16, 128, 336])
 def test_quantize_codes_and_scales_match_the_oracle_exactly(dtype, d, n):
     rng = np.random.default_rng(81)
     B, H = 1, 2

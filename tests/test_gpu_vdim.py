@@ -90,6 +90,20 @@ def test_key_blocks_and_dropout(kv_block, d, vw):
     _check_grads(grads, want, "bf16", f"dropout b={kv_block}")
 
 
+@pytest.mark.parametrize("n", [1, 129])
+@pytest.mark.parametrize("d,vw", [(64, 128), (128, 64)])
+def test_single_row_and_one_past_a_tile(n, d, vw):
+    B, H = 1, 3
+    wl, x = _inputs(B, H, n, d, vw, "bf16", "causal", 95)
+    mk, bits, _ = mask_for(wl)
+    status, o, lse, grads = _run(x, wl, "bf16", "causal", bits)
+    assert status == ea.ATTN_OK
+    Y, L = ref.forward(x["q"], x["k"], x["v"], wl.c, mk)
+    want = ref.backward(x["q"], x["k"], x["v"], wl.c, mk, x["do"])
+    check_forward(o, lse, Y, L, "bf16", f"n={n} v={vw}")
+    _check_grads(grads, want, "bf16", f"n={n} v={vw}")
+
+
 def test_several_tiles_and_heads():
     B, H, n, d, vw = 2, 2, 1024, 128, 64
     wl, x = _inputs(B, H, n, d, vw, "bf16", "none", 93)
