@@ -166,7 +166,8 @@ int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c,
  *   vt8     E4M3 [B][H][d][n]: V transposed (the value columns are rows), so that the P V
  *           product reads a K-major operand
  * The scores are c·q_scale·k_scale·(q8·k8) accumulated in float32.  Each probability enters the
- * P V product as an E4M3 value of 2^8 exp(s - m) (m the exact running maximum); the row sum
+ * P V product as an E4M3 value of 2^8 exp(s - m) (m the running maximum, at most 0.75 log2
+ * units below the true one, so the value stays below 448); the row sum
  * keeps the unrounded values.  The output therefore differs from exact attention on the
  * dequantized inputs by at most sum_j (2^-4 P_ij + 2^-18) |V_j| per element (the rounding of P),
  * plus float32 and bfloat16 rounding.  lse is float32, natural log, of the scaled scores.
