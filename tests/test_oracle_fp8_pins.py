@@ -150,3 +150,25 @@ def test_block_scaled_bound_covers_the_rounded_probabilities():
         Yq = (fp8.round_e4m3(P0 * h["r"][None, :]) @ (h["v8"] * svmax)) / P0.sum(axis=1, keepdims=True)
         assert np.all(np.abs(Yq - Y) <= bound * (1 + 1e-12) + 1e-15)
         assert np.max(np.abs(Yq - Y)) > 0
+
+
+def test_bound_holds_with_a_stale_running_maximum():
+    """The FP8 forward raises its running maximum only when a block's maximum exceeds it by more
+    than 0.75 in log2 units.  Brute force with the maximum anywhere in that window below the
+    true one: P' = 2^8 e^{s - m} stays below 448 (no saturation), and the output with P'
+    rounded to E4M3 stays within the same bound sum_j (2^-4 P_ij + 2^-18) |V_j|."""
+    rng = np.random.default_rng(26)
+    for trial in range(20):
+        n, d = 150, 16
+        q, k, v = rng.normal(size=(n, d)), rng.normal(size=(n, d)), rng.normal(size=(n, d))
+        a = rng.random((n, n)) < 0.5
+        a[np.arange(n), np.arange(n)] = True
+        c = 0.3 * (trial + 1)
+        Y, lse, bound = fp8.forward_rows_bound(q, k, v, c, a)
+        s = np.where(a, c * (q @ k.T), -np.inf)
+        lag = rng.uniform(0.0, 0.75, size=(n, 1)) * np.log(2.0)  # natural-log units
+        m = s.max(axis=1, keepdims=True) - lag
+        Pp = np.where(a, 256.0 * np.exp(s - m), 0.0)
+        assert Pp.max() < 448.0 and np.all(Pp.max(axis=1) >= 256.0)
+        Yq = (fp8.round_e4m3(Pp) @ v) / Pp.sum(axis=1, keepdims=True)
+        assert np.all(np.abs(Yq - Y) <= bound * (1 + 1e-12) + 1e-15)
