@@ -87,3 +87,40 @@ def test_backward_workspace_check_on_host(lib):
     rc = lib.attn_bwd(2, 2, 3, 1000, 64, 0.125, vp(16), vp(32), vp(48), vp(64), vp(80), vp(0),
                       0, vp(0), 0, 0, 0, vp(112), vp(128), vp(144), vp(160), need, vp(0))
     assert rc == -1
+
+
+def test_value_width_entries_reject_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+    fwd = lambda d, vw, o=64, p_drop=0.0: lib.attn_fwd_vdim(
+        2, 1, 1, 128, d, vw, 0.125, vp(16), vp(32), vp(48), 0, vp(0), 0, 0, 0, p_drop, 0, vp(o),
+        vp(80), vp(0))
+    assert fwd(64, 32) == -2 and fwd(128, 16) == -2 and fwd(64, 96) == -2  # pairs not built
+    assert fwd(64, 128, o=0) == -1          # null output (a supported pair gets that far)
+    assert fwd(128, 64, o=72) == -3         # misaligned output
+    assert fwd(64, 128, p_drop=1.0) == -1   # p_drop must lie in [0, 1)
+    bwd = lambda d, vw, ws=4096: lib.attn_bwd_vdim(
+        2, 1, 1, 128, d, vw, 0.125, vp(16), vp(32), vp(48), vp(64), vp(80), vp(96), 0, vp(0), 0,
+        0, 0, 0.0, 0, vp(112), vp(128), vp(144), vp(160), ws, vp(0))
+    assert bwd(64, 32) == -2
+    assert bwd(64, 128, ws=0) == -4         # workspace too small
+
+
+def test_fp8_block_entries_reject_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p
+    quant = lambda dtype=2, d=64, n=128, q=16, sq=256: lib.attn_fp8_quantize(
+        dtype, 1, 1, n, d, vp(q), vp(32), vp(48), vp(0), vp(64), vp(80), vp(96), vp(sq),
+        vp(272), vp(288), vp(0))
+    assert quant(dtype=0) == -2             # float32 inputs
+    assert quant(d=96) == -2 and quant(d=32) == -2
+    assert quant(n=100) == -2               # n not a multiple of 16
+    assert quant(q=0) == -1
+    assert quant(q=24) == -3                # misaligned input
+    assert quant(sq=258) == -3              # misaligned scales
+    fwd = lambda d=64, n=128, sk=272, o=64: lib.attn_fwd_fp8_blocks(
+        1, 1, n, d, 0.125, vp(16), vp(32), vp(48), vp(256), vp(sk), vp(288), 0, vp(0), 0, 0,
+        vp(o), vp(80), vp(0))
+    assert fwd(d=16) == -2
+    assert fwd(n=120) == -2
+    assert fwd(sk=0) == -1                  # null scale pointer
+    assert fwd(sk=274) == -3                # misaligned scale pointer
+    assert fwd(o=72) == -3
