@@ -1,14 +1,22 @@
 #!/usr/bin/env python3
-"""Benchmark of exact tiled attention on GB300: one step = forward + backward of the
-training-shaped workload (B=8, H=16, n=4096, d=128, bf16, no mask), i.e. every kernel of
-the path: forward (online softmax, writes O and LSE), backward preprocessing (D = rowsum
-dO∘O, cleared dQ accumulator), backward (recomputed P, dS; dQ, dK, dV) and dQ
-postprocessing.
+"""Benchmark of exact tiled attention on GB300.
 
-Prints ONE JSON line (rank 0).  FLOPs per step are counted the standard way: forward
-4·B·H·n²·d, backward 2.5 times that (10·B·H·n²·d), no mask so no causal factor.
+Headline step = forward + backward of the training-shaped workload (B=8, H=16, n=4096,
+d=128, bf16, no mask): three launches, every kernel of the path: the forward (online
+softmax; writes O and LSE), the dQ kernel (recomputes P and dS per query tile, computes
+D = rowsum(dO∘O) and writes the row table) and the dK/dV kernel (recomputes P and dS per key
+tile).  FLOPs per step are counted the standard way: forward 4·B·H·n²·d, backward 2.5 times
+that (10·B·H·n²·d), no mask so no causal factor.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+After the headline, the line's "workloads" list times every other configuration of the
+metric's range (n = 4096 ... 65536) the same way, each with its own roofline fraction and the
+oracle timed on a bounded sample beside it: the long-context causal forwards (n = 16384 and
+65536), the fp16 overflow shapes (d = 16 and 64, literal and hot scale), the block-sparse
+bitmap shape (bf16 and float32), the causal training shape and the small float32 shape.
+
+Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-legs]
 
 --impl reference times the CPU oracle (float64 numpy, materialised scores) on a bounded
 sample of the same workload.  Under torchrun with N > 1 every rank runs its own replica of
@@ -411,7 +419,202 @@ def run_ours(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    if world == 1 and not args.no_legs:
+        with ClockSampler(dev.index) as clk_legs:
+            line["workloads"] = run_legs(dev, stream, burst, hbm, line["clocks"].get("sm_max_mhz"))
+        line["workloads_clocks"] = clk_legs.summary()
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ other workloads
+# (workload, passes): every configuration of the metric's range beside the headline.
+LEGS = [
+    ("longctx_bf16_n16384", "fwd"),
+    ("longctx_bf16_n65536", "fwd"),
+    ("overflow_f16_d16", "fwd"),
+    ("overflow_f16_d16_hot", "fwd"),
+    ("overflow_f16_d64", "fwd"),
+    ("overflow_f16_d64_hot", "fwd"),
+    ("bitmap_bf16", "fwd+bwd"),
+    ("bitmap_f32", "fwd+bwd"),
+    ("train_bf16_d128_causal", "fwd+bwd"),
+    ("small_causal_f32", "fwd+bwd"),
+]
+MUFU_EX2_PER_CLK_SM = 32   # ex2.approx results per clock per SM (probed on this part)
+FFMA_PER_CLK_SM = 128      # float32 FMA lanes per SM
+N_SM = 152
+
+
+def leg_workload(name):
+    from synth import workload
+    if name == "train_bf16_d128_causal":
+        return workload("train_bf16_d128").with_(name=name, mask="causal")
+    return workload(name)
+
+
+def leg_mask(wl):
+    """(kappa, allowed [n, n] bool or None, device words or None)."""
+    import numpy as np
+    import torch
+    if wl.mask == "bitmap":
+        from synth import bitmap_mask, pack_bitmap
+        allowed = bitmap_mask(wl.n, wl.seed)
+        bits = torch.from_numpy(pack_bitmap(allowed).view(np.int32)).cuda()
+        return float(allowed.mean()), allowed, bits
+    return (0.5 if wl.mask == "causal" else 1.0), None, None
+
+
+def oracle_leg(wl, passes, allowed, row_budget=512):
+    """The oracle on a bounded sample of one head of the workload: (FLOP, seconds, sample).
+    Forward-only legs take evenly spaced query rows of head 0 (all keys they see); legs with a
+    backward take the whole head (the key gradients need every row)."""
+    import numpy as np
+    from oracle import attention as ref
+    from oracle import masks
+    from synth import draw_head
+    n, d = wl.n, wl.d
+    if allowed is not None:
+        mk = masks.dense(allowed)
+    else:
+        mk = masks.for_kind(wl.mask, n)
+    q, k, v = (draw_head(wl, t, 0) for t in ("q", "k", "v"))
+    if passes == "fwd":
+        rows = np.unique(np.linspace(0, n - 1, min(n, row_budget)).astype(np.int64))
+        a = mk(0, rows)
+        t0 = time.perf_counter()
+        ref.forward_rows(q[rows], k, v, wl.c, a)
+        dt = time.perf_counter() - t0
+        flop = 4.0 * float(a.sum()) * d
+        return flop, dt, f"{rows.size} evenly spaced query rows of 1 of {wl.heads} heads, forward"
+    g = draw_head(wl, "do", 0)
+    rows = np.arange(n)
+    a = mk(0, rows)
+    t0 = time.perf_counter()
+    ref.forward_rows(q, k, v, wl.c, a)
+    ref.backward_head(q, k, v, wl.c, a, g)
+    dt = time.perf_counter() - t0
+    return 14.0 * float(a.sum()) * d, dt, f"1 of {wl.heads} heads, forward + backward"
+
+
+def time_calls(fn, iters, flush, stream):
+    """Mean CUDA-event time (ms) of fn() over iters calls, L2 flushed before each call."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for i in range(iters):
+        flush.fill_(float(i))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def run_legs(dev, stream, burst, hbm, sm_mhz_max):
+    """Every other configuration of the metric's range, timed as the headline is (CUDA events
+    on the launching stream, L2 flushed between calls), with its roofline fractions and the
+    oracle on a bounded sample beside it."""
+    import torch
+    import exact_io_aware_gb300 as ea
+    flush = torch.empty(64 * 2**20, dtype=torch.float32, device=dev)  # 256 MiB > L2
+    dts = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+    clock_ghz = (sm_mhz_max or 2070.0) / 1e3
+    mufu_peak = MUFU_EX2_PER_CLK_SM * N_SM * clock_ghz * 1e9        # ex2 per second
+    ffma_peak = 2.0 * FFMA_PER_CLK_SM * N_SM * clock_ghz * 1e9 / 1e12  # float32 TFLOP/s
+    out = []
+    for name, passes in LEGS:
+        wl = leg_workload(name)
+        kappa, allowed, bits = leg_mask(wl)
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed)
+        shape = (wl.B, wl.H, wl.n, wl.d)
+        dt = dts[wl.dtype]
+        q, k, v, do = (torch.randn(shape, device=dev, generator=g) for _ in range(4))
+        q = (q * wl.q_scale).to(dt)
+        k, v, do = k.to(dt), v.to(dt), do.to(dt)
+        o = torch.empty_like(q)
+        lse = torch.empty(shape[:3], device=dev, dtype=torch.float32)
+        kvb = wl.kv_block
+        pairs = wl.heads * wl.n * wl.n * kappa
+        fwd_flop = 4.0 * pairs * wl.d
+        bwd_flop = 2.5 * fwd_flop
+        iters = 5 if wl.n >= 65536 else 20
+
+        def fwd():
+            ea.attn_fwd(q, k, v, wl.c, mask=wl.mask, mask_bits=bits, kv_block=kvb, o=o, lse=lse,
+                        stream=stream)
+
+        fwd_ms = time_calls(fwd, iters, flush, stream)
+        leg = {"workload": name, "B": wl.B, "H": wl.H, "n": wl.n, "d": wl.d, "dtype": wl.dtype,
+               "mask": wl.mask, "kappa": kappa, "passes": passes, "fwd_ms": fwd_ms,
+               "fwd_tflops": fwd_flop / (fwd_ms / 1e3) / 1e12}
+        splits = ea.attn_fwd_split_count(dt, wl.B, wl.H, wl.n, wl.d, kvb)
+        best_fwd_ms = fwd_ms
+        if splits > 1:
+            ws = torch.empty(max(16, ea.attn_fwd_split_workspace_bytes(dt, wl.B, wl.H, wl.n, wl.d,
+                                                                         splits)),
+                             dtype=torch.uint8, device=dev)
+
+            def fwd_split():
+                ea.attn_fwd_split(q, k, v, wl.c, mask=wl.mask, mask_bits=bits, kv_block=kvb,
+                                  num_splits=splits, o=o, lse=lse, workspace=ws, stream=stream)
+
+            leg["fwd_split_ms"] = time_calls(fwd_split, iters, flush, stream)
+            leg["fwd_split_shares"] = splits
+            best_fwd_ms = min(fwd_ms, leg["fwd_split_ms"])
+        step_ms = best_fwd_ms
+        step_flop = fwd_flop
+        if passes == "fwd+bwd":
+            fwd()
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws_b = torch.empty(ea.attn_bwd_workspace_bytes(dt, wl.B, wl.H, wl.n, wl.d),
+                               dtype=torch.uint8, device=dev)
+
+            def bwd():
+                ea.attn_bwd(q, k, v, o, lse, do, wl.c, mask=wl.mask, mask_bits=bits, kv_block=kvb,
+                            dq=dq, dk=dk, dv=dv, workspace=ws_b, stream=stream)
+
+            bwd_ms = time_calls(bwd, iters, flush, stream)
+            leg["bwd_ms"] = bwd_ms
+            leg["bwd_tflops"] = bwd_flop / (bwd_ms / 1e3) / 1e12
+            step_ms += bwd_ms
+            step_flop += bwd_flop
+        leg["status"] = ea.attn_device_status(stream)
+        leg["tflops"] = step_flop / (step_ms / 1e3) / 1e12
+        e = 4 if wl.dtype == "f32" else 2
+        fwd_bytes = wl.heads * (4.0 * wl.n * wl.d * e + 4.0 * wl.n)
+        frac = {}
+        if wl.dtype == "f32":
+            frac["fp32_alu"] = leg["tflops"] / ffma_peak
+        else:
+            frac["tensor"] = leg["tflops"] / burst
+        frac["hbm_fwd"] = fwd_bytes / (best_fwd_ms / 1e3) / 1e9 / hbm
+        frac["mufu_fwd"] = pairs / (best_fwd_ms / 1e3) / mufu_peak
+        bound = max(frac, key=frac.get)
+        leg["roofline"] = {
+            "fractions": frac, "highest": bound,
+            "peaks": {"tensor_tflops": burst, "hbm_gbs": hbm, "fp32_alu_tflops": ffma_peak,
+                      "mufu_ex2_per_s": mufu_peak},
+            "peak_source": "tensor and HBM measured (MEASURED_PEAKS.json); float32 FMA and ex2 "
+                           "rates = per-SM unit counts x 152 SMs x the maximum SM clock",
+            "algorithmic": "FLOP 4·B·H·n²·d·κ forward (2.5x backward); forward bytes "
+                           "4·n·d·e + 4n per head; one exp2 per allowed (query, key) pair",
+        }
+        try:
+            flop_c, dt_c, sample = oracle_leg(wl, passes, allowed)
+            leg["cpu_baseline"] = {"value": flop_c / dt_c / 1e12, "unit": "TFLOP/s",
+                                   "cores": _CORES, "kind": "oracle",
+                                   "sample": f"{sample}, {dt_c:.2f} s"}
+        except MemoryError:
+            leg["cpu_baseline"] = None
+        out.append(leg)
+        del q, k, v, do, o, lse
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -421,6 +624,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true",
+                    help="time the headline step only (no other workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

@@ -1,11 +1,13 @@
 // C ABI of the exact tiled attention library: argument checks, dispatch to the kernels,
 // error reporting and the device status word.  See include/exactattn.h for the contract.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "exactattn.h"
@@ -21,12 +23,30 @@ thread_local std::string g_last_error;
 __device__ uint32_t g_status_word;
 
 constexpr int kMaxDevices = 64;
-uint32_t* g_status_ptr[kMaxDevices] = {};
+
+// Per-device facts looked up once (std::call_once orders each lookup before every reader, so
+// host threads making their first calls at the same time neither race nor repeat it).
+struct DeviceInfo {
+  std::once_flag status_once, sm_once;
+  uint32_t* status = nullptr;
+  cudaError_t status_err = cudaSuccess;
+  int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
 
 int fail(int code, const std::string& msg) {
   g_last_error = msg;
   return code;
 }
+
+// An NVTX range named after the entry point, open for the length of the host call (the range
+// marks the call's argument checks and launches in a timeline; the kernels are asynchronous).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 int status_ptr(uint32_t** out) {
   int dev = 0;
@@ -37,14 +57,15 @@ int status_ptr(uint32_t** out) {
   // call and fails on a thread (an autograd worker, say) whose first CUDA call it would be.
   e = cudaSetDevice(dev);
   if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, std::string("cudaSetDevice: ") + cudaGetErrorString(e));
-  if (!g_status_ptr[dev]) {
+  DeviceInfo& info = g_dev[dev];
+  std::call_once(info.status_once, [&info] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_status_word);
-    if (e != cudaSuccess)
-      return fail(ATTN_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e));
-    g_status_ptr[dev] = static_cast<uint32_t*>(p);
-  }
-  *out = g_status_ptr[dev];
+    info.status_err = cudaGetSymbolAddress(&p, g_status_word);
+    info.status = info.status_err == cudaSuccess ? static_cast<uint32_t*>(p) : nullptr;
+  });
+  if (info.status_err != cudaSuccess || !info.status)
+    return fail(ATTN_ERR_CUDA, std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(info.status_err));
+  *out = info.status;
   return ATTN_OK;
 }
 
@@ -55,15 +76,14 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Streaming multiprocessors of the current device (looked up once per device).
 int sm_count() {
-  static int cached[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  if (!cached[dev]) {
+  DeviceInfo& info = g_dev[dev];
+  std::call_once(info.sm_once, [&info, dev] {
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = v;
-  }
-  return cached[dev];
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) info.sms = v;
+  });
+  return info.sms;
 }
 
 // Library choice of the key split (at most one share per key block and at most kMaxSplits).
@@ -255,6 +275,7 @@ extern "C" {
 int attn_fwd(int dtype, int B, int H, int n, int d, float c, const void* q, const void* k,
              const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
              int64_t mask_head_stride_words, int kv_block, void* o, float* lse, void* stream) {
+  CallRange range("attn_fwd");
   return fwd_general(dtype, B, H, n, n, d, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                      mask_head_stride_words, kv_block, 0.0f, 0, 1, o, lse, nullptr, 0, stream);
 }
@@ -263,6 +284,7 @@ int attn_fwd_dropout(int dtype, int B, int H, int n, int d, float c, const void*
                      const void* v, int mask_kind, const uint32_t* mask_bits,
                      int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                      float p_drop, uint64_t seed, void* o, float* lse, void* stream) {
+  CallRange range("attn_fwd_dropout");
   return fwd_general(dtype, B, H, n, n, d, d, c, q, k, v, mask_kind, mask_bits, mask_row_words,
                      mask_head_stride_words, kv_block, p_drop, seed, 1, o, lse, nullptr, 0,
                      stream);
@@ -289,6 +311,7 @@ int attn_fwd_split(int dtype, int B, int H, int n, int d, float c, const void* q
                    const void* v, int mask_kind, const uint32_t* mask_bits, int64_t mask_row_words,
                    int64_t mask_head_stride_words, int kv_block, int num_splits, void* o,
                    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  CallRange range("attn_fwd_split");
   if (num_splits < 0 || num_splits > kMaxSplits)
     return fail(ATTN_ERR_INVALID_ARG, "num_splits must be 0 (library choice) or 1..32");
   if (B < 1 || H < 1 || n < 1) return fail(ATTN_ERR_INVALID_ARG, "B, H and n must be positive");
@@ -303,6 +326,7 @@ int attn_fwd_kv(int dtype, int B, int H, int n_q, int n_kv, int d, float c, cons
                 int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                 int num_splits, void* o, float* lse, void* workspace, size_t workspace_bytes,
                 void* stream) {
+  CallRange range("attn_fwd_kv");
   if (num_splits < 0 || num_splits > kMaxSplits)
     return fail(ATTN_ERR_INVALID_ARG, "num_splits must be 0 (library choice) or 1..32");
   if (B < 1 || H < 1 || n_q < 1 || n_kv < 1)
@@ -317,6 +341,7 @@ int attn_fwd_fp8(int B, int H, int n, int d, float c, const void* q8, const void
                  const void* vt8, float q_scale, float k_scale, float v_scale, int mask_kind,
                  const uint32_t* mask_bits, int64_t mask_row_words,
                  int64_t mask_head_stride_words, void* o, float* lse, void* stream) {
+  CallRange range("attn_fwd_fp8");
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward supports d = 64 and 128");
   if (int rc = check_common(ATTN_BF16, B, H, n, d, q8, k8, vt8, mask_kind, mask_bits,
                             mask_row_words, mask_head_stride_words, 0))
@@ -346,6 +371,7 @@ int attn_fwd_fp8_blocks(int B, int H, int n, int d, float c, const void* q8, con
                         const float* v_scales, int mask_kind, const uint32_t* mask_bits,
                         int64_t mask_row_words, int64_t mask_head_stride_words, void* o,
                         float* lse, void* stream) {
+  CallRange range("attn_fwd_fp8_blocks");
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward supports d = 64 and 128");
   if (int rc = check_common(ATTN_BF16, B, H, n, d, q8, k8, vt8, mask_kind, mask_bits,
                             mask_row_words, mask_head_stride_words, 0))
@@ -375,6 +401,7 @@ int attn_fwd_fp8_blocks(int B, int H, int n, int d, float c, const void* q8, con
 int attn_fp8_quantize(int dtype, int B, int H, int n, int d, const void* q, const void* k,
                       const void* v, const int8_t* signs, void* q8, void* k8, void* vt8,
                       float* q_scales, float* k_scales, float* v_scales, void* stream) {
+  CallRange range("attn_fp8_quantize");
   if (dtype != ATTN_BF16 && dtype != ATTN_F16)
     return fail(ATTN_ERR_UNSUPPORTED, "the FP8 quantization reads bf16 or fp16 inputs");
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "the FP8 quantization supports d = 64 and 128");
@@ -400,6 +427,7 @@ int attn_fp8_quantize(int dtype, int B, int H, int n, int d, const void* q, cons
 
 int attn_merge(int dtype, int num_parts, int64_t rows, int d, const float* o_parts,
                const float* lse_parts, void* o, float* lse, void* stream) {
+  CallRange range("attn_merge");
   if (dtype < ATTN_F32 || dtype > ATTN_BF16) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype");
   if (num_parts < 1 || rows < 1 || d < 4)
     return fail(ATTN_ERR_INVALID_ARG, "num_parts and rows must be positive and d >= 4");
@@ -478,6 +506,7 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c, const void* q, cons
              const uint32_t* mask_bits, int64_t mask_row_words, int64_t mask_head_stride_words,
              int kv_block, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
              void* stream) {
+  CallRange range("attn_bwd");
   return bwd_impl(dtype, B, H, n, d, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
                   mask_row_words, mask_head_stride_words, kv_block, 0.0f, 0, dq, dk, dv,
                   workspace, workspace_bytes, stream);
@@ -489,6 +518,7 @@ int attn_bwd_dropout(int dtype, int B, int H, int n, int d, float c, const void*
                      int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                      float p_drop, uint64_t seed, void* dq, void* dk, void* dv, void* workspace,
                      size_t workspace_bytes, void* stream) {
+  CallRange range("attn_bwd_dropout");
   return bwd_impl(dtype, B, H, n, d, d, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
                   mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, dq, dk, dv,
                   workspace, workspace_bytes, stream);
@@ -498,6 +528,7 @@ int attn_fwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c, con
                   const void* k, const void* v, int mask_kind, const uint32_t* mask_bits,
                   int64_t mask_row_words, int64_t mask_head_stride_words, int kv_block,
                   float p_drop, uint64_t seed, void* o, float* lse, void* stream) {
+  CallRange range("attn_fwd_vdim");
   return fwd_general(dtype, B, H, n, n, d, v_dim, c, q, k, v, mask_kind, mask_bits,
                      mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, 1, o, lse,
                      nullptr, 0, stream);
@@ -509,12 +540,14 @@ int attn_bwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c, con
                   int64_t mask_head_stride_words, int kv_block, float p_drop, uint64_t seed,
                   void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                   void* stream) {
+  CallRange range("attn_bwd_vdim");
   return bwd_impl(dtype, B, H, n, d, v_dim, c, q, k, v, o, lse, d_o, mask_kind, mask_bits,
                   mask_row_words, mask_head_stride_words, kv_block, p_drop, seed, dq, dk, dv,
                   workspace, workspace_bytes, stream);
 }
 
 int attn_device_status(void* stream) {
+  CallRange range("attn_device_status");
   uint32_t* p = nullptr;
   if (int rc = status_ptr(&p)) return rc;
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
@@ -535,6 +568,7 @@ int attn_device_status(void* stream) {
 }
 
 int attn_selftest_wait_timeout(void* stream) {
+  CallRange range("attn_selftest_wait_timeout");
   uint32_t* st = nullptr;
   if (int rc = status_ptr(&st)) return rc;
   selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st);

@@ -14,7 +14,10 @@
 //    problems are rejected with ATTN_ERR_WORKSPACE before anything is launched.
 //  * The first call on each device looks up the array's device address with
 //    cudaGetSymbolAddress while that device is current; make that first call before any
-//    stream capture on the device.
+//    stream capture on the device.  The lookup runs once per device for the life of the
+//    process (std::call_once, so host threads making their first calls at the same time are
+//    safe) and its result is kept: after cudaDeviceReset the library's module is gone and
+//    this entry point must not be used again in that process.
 //  * All calls share the one array and it keeps the last call's contents.  Each call rewrites
 //    the whole table before reading it, so stale contents never leak into results,
 //    but two calls whose work overlaps on the GPU (different streams, no ordering between
@@ -24,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 #include "exactattn.h"
@@ -36,9 +40,18 @@ constexpr size_t kScratchBytes = ATTN_BWD_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_bwd_scratch on the current device (looked up once per device).
+// The array's device address on one device, looked up once.  std::call_once orders the
+// lookup before every reader, so concurrent first calls from several host threads neither
+// race nor look it up twice.
+struct DeviceScratch {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+DeviceScratch g_scratch[kMaxDevices];
+
+// Device address of g_bwd_scratch on the current device.
 int scratch_ptr(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -50,16 +63,17 @@ int scratch_ptr(void** out) {
     ea::set_last_error("device ordinal too large");
     return ATTN_ERR_UNSUPPORTED;
   }
-  if (!g_scratch_ptr[dev]) {
+  DeviceScratch& s = g_scratch[dev];
+  std::call_once(s.once, [&s] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      ea::set_last_error(std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(e));
-      return ATTN_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
+    s.err = cudaGetSymbolAddress(&p, g_bwd_scratch);
+    s.ptr = s.err == cudaSuccess ? p : nullptr;
+  });
+  if (s.err != cudaSuccess || s.ptr == nullptr) {
+    ea::set_last_error(std::string("cudaGetSymbolAddress(scratch): ") + cudaGetErrorString(s.err));
+    return ATTN_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return ATTN_OK;
 }
 

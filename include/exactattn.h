@@ -333,7 +333,9 @@ int attn_bwd_vdim(int dtype, int B, int H, int n, int d, int v_dim, float c,
  * until the process exits.  A problem with attn_bwd_workspace_bytes(...) larger than that
  * is rejected with ATTN_ERR_WORKSPACE (see attn_last_error) before anything runs.  The first
  * call on a device looks up the array's address on that device (cudaGetSymbolAddress); make
- * it before any stream capture there.  All calls share the array, which keeps the last
+ * it before any stream capture there.  The lookup happens once per device per process (safe
+ * when several host threads make their first call at once) and is kept, so the entry point
+ * must not be used after cudaDeviceReset in the same process.  All calls share the array, which keeps the last
  * call's contents; each call rewrites the table before reading it, but calls that overlap on the
  * GPU (unordered streams) race on it.  No cudaMalloc, cudaFree or allocating library call is
  * made.  Other arguments, outputs and errors as for attn_bwd.

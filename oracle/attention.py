@@ -65,8 +65,9 @@ def forward(Q, K, V, c, mask, heads=None):
     return Y, L
 
 
-def backward_head(q, k, v, c, allowed, g):
-    """dQ, dK, dV of Φ = Σ G∘Y for one head, plus the forward's Y and LSE."""
+def probabilities_and_gamma(q, k, v, c, allowed, g):
+    """p [n,n] and γ [n,n] of one head (the reverse map's per-element quantities), plus the
+    forward's Y and LSE.  Both are exactly 0 where the key is not allowed."""
     y, lse, _, _ = forward_rows(q, k, v, c, allowed)
     s = masked_scores(q, k, c, allowed)
     finite = np.isfinite(lse)
@@ -76,6 +77,13 @@ def backward_head(q, k, v, c, allowed, g):
     delta = (g * y).sum(axis=1)
     dp = g @ _f64(v).T
     gamma = p * (dp - delta[:, None])
+    return p, gamma, y, lse
+
+
+def backward_head(q, k, v, c, allowed, g):
+    """dQ, dK, dV of Φ = Σ G∘Y for one head, plus the forward's Y and LSE."""
+    p, gamma, y, lse = probabilities_and_gamma(q, k, v, c, allowed, g)
+    g = _f64(g)
     dq = float(c) * (gamma @ _f64(k))
     dk = float(c) * (gamma.T @ _f64(q))
     dv = p.T @ g

@@ -72,15 +72,15 @@ def check_forward(o, lse, Y, L, dtype, what=""):
 
 
 def rel_frob_per_head(got, want):
-    """||got - want||_F / max(||want||_F, 1) per head.  The floor of 1 turns the measure into
-    an absolute one where the exact gradient (nearly) vanishes, e.g. n = 1, where every
-    probability is 1 and dQ = dK = 0 exactly."""
+    """||got - want||_F / ||want||_F per head: the relative Frobenius error the tolerance is
+    stated in.  Only a head whose exact gradient is identically zero (e.g. n = 1, where every
+    probability is 1 and dQ = dK = 0 exactly) is measured absolutely, ||got||_F."""
     got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
     g = got.reshape(-1, *got.shape[-2:])
     w = want.reshape(-1, *want.shape[-2:])
     num = np.linalg.norm((g - w).reshape(g.shape[0], -1), axis=1)
     den = np.linalg.norm(w.reshape(w.shape[0], -1), axis=1)
-    return num / np.maximum(den, 1.0)
+    return num / np.where(den == 0.0, 1.0, den)
 
 
 def check_grads(grads, refs, dtype, what=""):

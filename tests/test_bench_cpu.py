@@ -47,3 +47,25 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_every_leg_names_a_workload_and_counts_allowed_pairs():
+    import numpy as np
+    from synth import bitmap_mask
+    for name, passes in bench.LEGS:
+        wl = bench.leg_workload(name)
+        assert wl.name == name and passes in ("fwd", "fwd+bwd")
+    assert bench.leg_workload("train_bf16_d128_causal").mask == "causal"
+    # causal fwd+bwd over the whole head: 14 FLOP per allowed pair per column, n(n+1)/2 pairs
+    wl = bench.leg_workload("small_causal_f32")
+    flop, dt, sample = bench.oracle_leg(wl, "fwd+bwd", None)
+    assert flop == 14.0 * (256 * 257 / 2) * 64 and dt > 0 and "forward + backward" in sample
+    # forward-only legs sample evenly spaced rows; the last row sees every key
+    wl = bench.leg_workload("longctx_bf16_n16384")
+    flop, _, sample = bench.oracle_leg(wl, "fwd", None, row_budget=3)
+    assert flop == 4.0 * (1 + 8192 + 16384) * 128 and sample.startswith("3 evenly spaced")
+    wl = bench.leg_workload("bitmap_f32")
+    allowed = bitmap_mask(wl.n, wl.seed)
+    flop, _, _ = bench.oracle_leg(wl, "fwd", allowed, row_budget=2)
+    assert flop == 4.0 * (allowed[0].sum() + allowed[-1].sum()) * 64
+    assert 0.3 < float(np.mean(allowed)) < 0.5

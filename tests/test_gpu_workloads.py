@@ -96,7 +96,8 @@ def test_training_workload_forward_and_backward():
     rng = np.random.default_rng(3)
     mk = masks.none(wl.n)
     _check_rows(wl, o, lse, mk, [0, 37, 127], _sample_rows(wl.n, rng, 256))
-    for bh in (5, 122):
+    # eight heads spread over both batch rows and every head index range, compared whole
+    for bh in (0, 5, 19, 46, 63, 77, 100, 122):
         b, h = divmod(bh, wl.H)
         q, k, v, g = (draw_head(wl, t, bh) for t in ("q", "k", "v", "do"))
         rq, rk, rv, _, _ = ref.backward_head(q, k, v, wl.c, mk(bh, np.arange(wl.n)), g)

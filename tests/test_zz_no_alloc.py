@@ -3,20 +3,20 @@
 Engines that own every device allocation, or systems that freeze their memory budget at
 start-up, cannot hand the backward a freshly allocated workspace.  attn_bwd_noalloc takes its
 float32 scratch from a fixed static array in the library instead.  This file checks, through
-the C ABI, that it returns what attn_bwd returns (within the tolerances the other tests use)
-on two calls in a row, that it allocates no device memory, and that it refuses problems
-larger than its array.  It is collected last on purpose.
+the C ABI, that on two calls in a row with different inputs it returns bit for bit what
+attn_bwd returns on the same inputs (the same kernels run; only the scratch differs, so a
+stale or aliased table would show as a changed bit), that it allocates no device memory, and
+that it refuses problems larger than its array.  It is collected last on purpose.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 import exact_io_aware_gb300 as ea
 from synth import Workload
 
-from helpers import head_inputs, rel_frob_per_head, to_dev, tol_grad
+from helpers import head_inputs, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -34,32 +34,43 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _free_device_bytes_unchanged(before, tries=3):
+    """True if the device's free memory is back at `before` in one of a few readings (another
+    process on a shared GPU may move it for a moment; a leak by this call would not go away)."""
+    for _ in range(tries):
+        torch.cuda.synchronize()
+        if torch.cuda.mem_get_info()[0] >= before:
+            return True
+    return False
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_noalloc_matches_attn_bwd_on_two_calls(dtype):
     lib = ea.load()
     noalloc = _noalloc(lib)
-    wl = Workload("noalloc", 21, 2, 3, 777, 64, dtype, "causal", 0.125)
-    inp = head_inputs(wl)
-    dev = {t: to_dev(inp[t], dtype) for t in inp}
-    q, k, v, g = dev["q"], dev["k"], dev["v"], dev["do"]
-    o, lse = ea.attn_fwd(q, k, v, wl.c, mask="causal")
-    ref = ea.attn_bwd(q, k, v, o, lse, g, wl.c, mask="causal")
-    code = ea.DTYPE_CODE[q.dtype]
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    outs = [tuple(torch.full_like(q, float("nan")) for _ in range(3)) for _ in range(2)]
-    torch.cuda.synchronize()
-    for call, (dq, dk, dv) in enumerate(outs):
+    # two problems of different shapes and seeds, run back to back through the one array
+    for call, (seed, H, n) in enumerate(((21, 3, 777), (22, 2, 300))):
+        wl = Workload("noalloc", seed, 2, H, n, 64, dtype, "causal", 0.125)
+        inp = head_inputs(wl)
+        dev = {t: to_dev(inp[t], dtype) for t in inp}
+        q, k, v, g = dev["q"], dev["k"], dev["v"], dev["do"]
+        o, lse = ea.attn_fwd(q, k, v, wl.c, mask="causal")
+        ref = ea.attn_bwd(q, k, v, o, lse, g, wl.c, mask="causal")
+        code = ea.DTYPE_CODE[q.dtype]
+        dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+        torch.cuda.synchronize()
+        torch_bytes = torch.cuda.memory_allocated()
         free_before = torch.cuda.mem_get_info()[0]
         rc = noalloc(code, wl.B, wl.H, wl.n, wl.d, wl.c, _p(q), _p(k), _p(v), _p(o), _p(lse),
                      _p(g), 1, ctypes.c_void_p(0), 0, 0, 0, _p(dq), _p(dk), _p(dv), stream)
         assert rc == 0, ea.attn_last_error()
         assert ea.attn_device_status() == ea.ATTN_OK
+        assert torch.cuda.memory_allocated() == torch_bytes
         if call == 1:  # the first call may load the library's module data on this device
-            assert torch.cuda.mem_get_info()[0] == free_before
-        for got, want in zip((dq, dk, dv), ref):
-            err = rel_frob_per_head(got, want.double().cpu().numpy())
-            assert torch.isfinite(got).all()
-            assert err.max() <= tol_grad(dtype)
+            assert _free_device_bytes_unchanged(free_before)
+        for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+            assert torch.equal(got, want), f"call {call}: {name} differs from attn_bwd"
 
 
 def test_noalloc_refuses_problems_larger_than_its_scratch():
