@@ -25,7 +25,8 @@ __all__ = [
     "library_path", "load", "attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes",
     "attn_device_status", "attn_last_error", "attention", "attn_bwd_noalloc",
     "attn_selftest_wait_timeout", "attn_fwd_split", "attn_fwd_split_count",
-    "attn_fwd_split_workspace_bytes", "attn_merge",
+    "attn_fwd_split_workspace_bytes", "attn_merge", "attn_selftest_exp2",
+    "attn_debug_set_ring_stages",
 ]
 
 
@@ -112,6 +113,10 @@ def load():
     lib.attn_bwd_dropout.argtypes = [i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, i32,
                                      vp, i64, i64, i32, f32, u64, vp, vp, vp, vp, sz, vp]
     lib.attn_bwd_dropout.restype = i32
+    lib.attn_selftest_exp2.argtypes = [vp, vp, vp, i64, vp]
+    lib.attn_debug_set_ring_stages.argtypes = [i32]
+    lib.attn_debug_set_ring_stages.restype = i32
+    lib.attn_selftest_exp2.restype = i32
     _lib = lib
     return lib
 
@@ -473,6 +478,22 @@ def attn_selftest_wait_timeout(stream=None) -> int:
     lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_void_p]
     lib.attn_selftest_wait_timeout.restype = ctypes.c_int
     return _check(lib.attn_selftest_wait_timeout(_stream_ptr(stream)))
+
+
+def attn_selftest_exp2(x, stream=None):
+    """(2^x on the FMA pipe, 2^x on the MUFU unit) for a float32 CUDA tensor x (attn_selftest_exp2)."""
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y_fma, y_mufu = torch.empty_like(x), torch.empty_like(x)
+    _check(load().attn_selftest_exp2(_ptr(x), _ptr(y_fma), _ptr(y_mufu), x.numel(),
+                                     _stream_ptr(stream)))
+    return y_fma, y_mufu
+
+
+def attn_debug_set_ring_stages(stages: int) -> None:
+    """Cap every kernel's shared-memory ring depth at ``stages`` (0 = default); a testing aid:
+    results are bit for bit the same at every depth (attn_debug_set_ring_stages)."""
+    _check(load().attn_debug_set_ring_stages(int(stages)))
 
 
 def attn_device_status(stream=None) -> int:

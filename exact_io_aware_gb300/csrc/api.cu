@@ -4,6 +4,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -17,6 +18,9 @@
 namespace {
 
 thread_local std::string g_last_error;
+
+// Cap on every kernel's shared-memory ring depth (attn_debug_set_ring_stages; 0 = none).
+std::atomic<int> g_ring_stages{0};
 
 // One status word per device, in static device memory (no allocation).  Kernels OR flags
 // into it; attn_device_status reads and clears it.
@@ -176,6 +180,7 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.kv_block = kv_block;
   a.num_splits = 1;
   a.nk = n;
+  a.ring_stages = g_ring_stages.load(std::memory_order_relaxed);
   return a;
 }
 
@@ -195,6 +200,15 @@ __global__ void selftest_wait_kernel(uint32_t* status) {
   }
   __syncwarp();
   ea::mbar_wait(&bar, 0, status, 0x3F);
+}
+
+// y_fma[i] = ex2_fma(x[i]) (FMA pipe), y_mufu[i] = ex2.approx.ftz(x[i]) (MUFU unit).
+__global__ void selftest_exp2_kernel(const float* x, float* y_fma, float* y_mufu, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    y_fma[i] = ea::ex2_fma(x[i]);
+    y_mufu[i] = ea::ex2(x[i]);
+  }
 }
 
 }  // namespace
@@ -255,6 +269,8 @@ int fwd_general(int dtype, int B, int H, int nq, int nk, int d, int v_dim, float
                                           split_part_bytes(B, H, nq, v_dim, splits));
   }
   if (int rc = status_ptr(&a.status)) return rc;
+  if (a.ring_stages != 0 && dtype == ATTN_F32)
+    return fail(ATTN_ERR_UNSUPPORTED, "a ring-depth cap applies to the tensor-core kernels");
   std::string err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc = dtype == ATTN_F32 ? ea::launch_fwd_f32(a, s, err)
@@ -489,6 +505,8 @@ int bwd_impl(int dtype, int B, int H, int n, int d, int v_dim, float c, const vo
   a.workspace_bytes = workspace_bytes;
   if (int rc = set_dropout(p_drop, seed, a)) return rc;
   if (int rc = status_ptr(&a.status)) return rc;
+  if (a.ring_stages != 0 && dtype == ATTN_F32)
+    return fail(ATTN_ERR_UNSUPPORTED, "a ring-depth cap applies to the tensor-core kernels");
   std::string err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int rc = dtype == ATTN_F32 ? ea::launch_bwd_f32(a, s, err)
@@ -575,6 +593,26 @@ int attn_selftest_wait_timeout(void* stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(ATTN_ERR_CUDA, std::string("self-test launch: ") + cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+int attn_selftest_exp2(const float* x, float* y_fma, float* y_mufu, int64_t n, void* stream) {
+  CallRange range("attn_selftest_exp2");
+  if (n < 0) return fail(ATTN_ERR_INVALID_ARG, "n must be non-negative");
+  if (n == 0) return ATTN_OK;
+  if (!x || !y_fma || !y_mufu) return fail(ATTN_ERR_INVALID_ARG, "null pointer");
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+  selftest_exp2_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      x, y_fma, y_mufu, n);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, std::string("exp2 self-test launch: ") + cudaGetErrorString(e));
+  return ATTN_OK;
+}
+
+int attn_debug_set_ring_stages(int stages) {
+  if (stages < 0 || stages > 4) return fail(ATTN_ERR_INVALID_ARG, "ring stages must be 0 .. 4");
+  g_ring_stages.store(stages, std::memory_order_relaxed);
   return ATTN_OK;
 }
 

@@ -69,6 +69,8 @@ struct BwdParams {
   const void* q;
   uint32_t* status;
   DropoutArgs drop;  // read only by the dropout instantiations
+  Ring ring_q;          // depth of the dK/dV kernel's (Q, dO, row table) ring
+  Ring ring_k, ring_v;  // depths of the dQ kernel's K and V rings
 };
 
 __host__ __device__ constexpr int pad32(int x) { return x < 32 ? 32 : x; }
@@ -162,7 +164,8 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   }
 }
 
-template <bool kBf16, int D, int DV, bool kDrop>
+// kCap: ring depth from the launch (p.ring_q) instead of the compile-time count.
+template <bool kBf16, int D, int DV, bool kDrop, bool kCap = false>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TQ = typename C::TQ;
   using TG = typename C::TG;
   constexpr int NS = C::NS;
+  const auto ring_q = ring_of<kCap, NS>(p.ring_q);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -290,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sV + b * TV::kBoxBytes, &tm_v, &bars.kv_full, b * TV::L::kBoxCols, key0, bh);
     }
     for (int i = 0; i < nsteps; ++i) {
-      const int s = i % NS;
+      const int s = ring_q.stage(i);
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
-      if (!mbar_wait_spin(&bars.qdo_empty[s], ((i / NS) & 1) ^ 1, p.status, 21)) break;
+      if (!mbar_wait_spin(&bars.qdo_empty[s], ring_q.parity(i) ^ 1, p.status, 21)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars.qdo_full[s], TQ::kBytes + TG::kBytes);
 #pragma unroll
@@ -343,10 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dqmn0 = TQ::desc_mn(smem_u32(sQ), 0), dgmn0 = TG::desc_mn(smem_u32(sG), 0);
     bool ok = mbar_wait_spin_warp(&bars.kv_full, 0, p.status, 22);
     auto wait_qdo = [&](int i) -> bool {
-      return mbar_wait_spin_warp(&bars.qdo_full[i % NS], (i / NS) & 1, p.status, 23);
+      return mbar_wait_spin_warp(&bars.qdo_full[ring_q.stage(i)], ring_q.parity(i), p.status, 23);
     };
     auto issue_s = [&](int i) {
-      const uint64_t dq = dq0 + static_cast<uint64_t>(i % NS) * kStage;
+      const uint64_t dq = dq0 + static_cast<uint64_t>(ring_q.stage(i)) * kStage;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     auto issue_dp = [&](int i) {
-      const uint64_t dg = dg0 + static_cast<uint64_t>(i % NS) * kStageG;
+      const uint64_t dg = dg0 + static_cast<uint64_t>(ring_q.stage(i)) * kStageG;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     for (int i = 0; i < nsteps && ok; ++i) {
-      const int s = i % NS;
+      const int s = ring_q.stage(i);
       ok = mbar_wait_spin_warp(&bars.p_full, i & 1, p.status, 24);
       if (!ok) break;
       tc_fence_after();
@@ -425,9 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nsteps && ok; ++i) {
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
       const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
-      const float* L = sL + (i % NS) * BQ;
-      const float* Dd = sD + (i % NS) * BQ;
-      ok = mbar_wait_spin(&bars.ld_full[i % NS], (i / NS) & 1, p.status, 32);
+      const int stg = ring_q.stage(i);
+      const float* L = sL + stg * BQ;
+      const float* Dd = sD + stg * BQ;
+      ok = mbar_wait_spin(&bars.ld_full[stg], ring_q.parity(i), p.status, 32);
       if (!ok) break;
       // Dropout: keep bits of this key with the warp's query columns (bit k of word h <->
       // query q0 + c_lo + 32 h + k), drawn while the scores are still being computed.  One
@@ -478,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (partial) {
           if (p.mask_kind == kMaskBitmap) {
             // this warp's 32 keys share one word per query row (staged by the producer)
-            const uint32_t* wb = sBits + ((i % NS) * BQ + c0) * 4 + quad;
+            const uint32_t* wb = sBits + (stg * BQ + c0) * 4 + quad;
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               if (!((wb[4 * k] >> lane) & 1u)) pv[k] = 0.0f;

@@ -10,7 +10,7 @@ namespace bwd {
 
 constexpr int kMaxDynSmem = 227 * 1024 - 1024;
 
-template <bool kBf16, int D, int DV, bool kDrop>
+template <bool kBf16, int D, int DV, bool kDrop, bool kCap = false>
 int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   using Cfg = Config<D, DV>;
   using QCfg = dq::Config<D, DV>;
@@ -41,9 +41,14 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
               L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.q,
               a.status};
   p.drop = a.drop;
+  // the dK/dV kernel issues S_{i+1} before dK_i releases stage i, and the dQ kernel S_{i+1}
+  // before dQ_i releases K_i: those rings need two stages
+  p.ring_q = Ring::make(ring_depth(a.ring_stages, 2, Cfg::NS));
+  p.ring_k = Ring::make(ring_depth(a.ring_stages, 2, QCfg::NSK));
+  p.ring_v = Ring::make(ring_depth(a.ring_stages, 1, QCfg::NSV));
   const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
   // the dQ kernel writes the row table the dK/dV kernel reads
-  auto qkern = dq::dq_tc_kernel<kBf16, D, DV, kDrop>;
+  auto qkern = dq::dq_tc_kernel<kBf16, D, DV, kDrop, kCap>;
   cudaError_t e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(qsmem));
   if (e == cudaSuccess) {
@@ -54,7 +59,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
     err = std::string("dQ launch: ") + cudaGetErrorString(e);
     return -5;
   }
-  auto kern = bwd_tc_kernel<kBf16, D, DV, kDrop>;
+  auto kern = bwd_tc_kernel<kBf16, D, DV, kDrop, kCap>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem));
   if (e == cudaSuccess) {
@@ -71,6 +76,14 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
 // Instantiations with and without dropout for one (key width, value width) pair.
 template <int D, int DV = D>
 int run_d(bool bf16, const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
+  if (a.ring_stages != 0) {
+    // ring depths from the launch: one instantiation, as a testing aid
+    if constexpr (D == 128 && DV == 128) {
+      if (bf16 && !a.dropout) return run<true, 128, 128, false, true>(a, table, s, err);
+    }
+    err = "a ring-depth cap applies to bf16, d = v = 128, without dropout";
+    return -2;
+  }
   if (a.dropout)
     return bf16 ? run<true, D, DV, true>(a, table, s, err) : run<false, D, DV, true>(a, table, s, err);
   return bf16 ? run<true, D, DV, false>(a, table, s, err) : run<false, D, DV, false>(a, table, s, err);

@@ -126,7 +126,8 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&w)[N]) 
   }
 }
 
-template <bool kBf16, int D, int DV, bool kDrop>
+// kCap: ring depths from the launch (p.ring_k, p.ring_v) instead of the compile-time counts.
+template <bool kBf16, int D, int DV, bool kDrop, bool kCap = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_dq, bwd::BwdParams p) {
@@ -136,6 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   using TV = typename C::TV;
   constexpr int NSK = C::NSK;
   constexpr int NSV = C::NSV;
+  const auto ring_k = ring_of<kCap, NSK>(p.ring_k);
+  const auto ring_v = ring_of<kCap, NSV>(p.ring_v);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = bwd::align1024(smem_raw);
@@ -247,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       for (int i = 0; i < nsteps; ++i) {
-        const int s = i % NSK;
-        if (!mbar_wait_spin(&bars.k_empty[s], ((i / NSK) & 1) ^ 1, p.status, 42)) break;
+        const int s = ring_k.stage(i);
+        if (!mbar_wait_spin(&bars.k_empty[s], ring_k.parity(i) ^ 1, p.status, 42)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], TK::kBytes);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b)
@@ -267,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA producer: V
     if (lane == 0) {
       for (int i = 0; i < nsteps; ++i) {
-        const int s = i % NSV;
-        if (!mbar_wait_spin(&bars.v_empty[s], ((i / NSV) & 1) ^ 1, p.status, 41)) break;
+        const int s = ring_v.stage(i);
+        if (!mbar_wait_spin(&bars.v_empty[s], ring_v.parity(i) ^ 1, p.status, 41)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], TV::kBytes);
 #pragma unroll
         for (int b = 0; b < TV::L::kBoxes; ++b)
@@ -289,9 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dkmn0 = TK::desc_mn(smem_u32(sK), 0);
     bool ok = nsteps == 0 || mbar_wait_spin_warp(&bars.qg_full, 0, p.status, 43);
     auto issue_s = [&](int i) -> bool {
-      if (!mbar_wait_spin_warp(&bars.k_full[i % NSK], (i / NSK) & 1, p.status, 44)) return false;
+      const int ks = ring_k.stage(i);
+      if (!mbar_wait_spin_warp(&bars.k_full[ks], ring_k.parity(i), p.status, 44)) return false;
       tc_fence_after();
-      const uint64_t dk = dk0 + static_cast<uint64_t>(i % NSK) * kStage;
+      const uint64_t dk = dk0 + static_cast<uint64_t>(ks) * kStage;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
@@ -302,16 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     auto issue_dp = [&](int i) -> bool {
-      if (!mbar_wait_spin_warp(&bars.v_full[i % NSV], (i / NSV) & 1, p.status, 45)) return false;
+      const int vs = ring_v.stage(i);
+      if (!mbar_wait_spin_warp(&bars.v_full[vs], ring_v.parity(i), p.status, 45)) return false;
       tc_fence_after();
-      const uint64_t dv = dv0 + static_cast<uint64_t>(i % NSV) * kStageV;
+      const uint64_t dv = dv0 + static_cast<uint64_t>(vs) * kStageV;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < DV / 16; ++kk)
           mma_ts(tmem + C::kColDP, tmem + C::kColG + kk * 8, dv + TV::k_step(kk), id_s,
                  kk > 0 ? 1u : 0u);
         mma_commit(&bars.dp_full);
-        mma_commit(&bars.v_empty[i % NSV]);
+        mma_commit(&bars.v_empty[vs]);
       }
       __syncwarp();
       return true;
@@ -329,13 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 46);
       if (!ok) break;
       tc_fence_after();
-      const uint64_t dkmn = dkmn0 + static_cast<uint64_t>(i % NSK) * kStage;
+      const int ks = ring_k.stage(i);
+      const uint64_t dkmn = dkmn0 + static_cast<uint64_t>(ks) * kStage;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tmem + C::kColDQ, tmem + C::kColDP + packed_col(16 * kk), dkmn + TK::mn_step(kk),
                  id_q, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.k_empty[i % NSK]);
+        mma_commit(&bars.k_empty[ks]);
       }
       __syncwarp();
       // dP_{i+1} overwrites dS_i, which dQ_i (issued before it) has read

@@ -7,7 +7,7 @@
 namespace ea {
 namespace fp8 {
 
-template <int D, bool kBlocks>
+template <int D, bool kBlocks, bool kCap = false>
 int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, const float* sq_blk,
         const float* sk_blk, const float* sv_blk, cudaStream_t s, std::string& err) {
   using Cfg = Config<D>;
@@ -24,7 +24,7 @@ int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, const 
     err = "cuTensorMapEncodeTiled rejected an FP8 tensor map";
     return -5;
   }
-  auto kern = fwd_fp8_kernel<D, kBlocks>;
+  auto kern = fwd_fp8_kernel<D, kBlocks, kCap>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
@@ -44,6 +44,7 @@ int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, const 
            sq_blk,
            sk_blk,
            sv_blk};
+  p.ring = Ring::make(ring_depth(a.ring_stages, 1, Config<D>::NS));
   dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   e = cudaGetLastError();
@@ -59,6 +60,13 @@ int run(const AttnArgs& a, const void* vt8, float sq, float sk, float sv, const 
 int launch_fwd_fp8(const AttnArgs& a, const void* vt8, float sq, float sk, float sv,
                    const float* sq_blk, const float* sk_blk, const float* sv_blk, cudaStream_t s,
                    std::string& err) {
+  if (a.ring_stages != 0) {
+    // ring depth from the launch: one instantiation, as a testing aid
+    if (a.d == 128 && !sk_blk)
+      return fp8::run<128, false, true>(a, vt8, sq, sk, sv, sq_blk, sk_blk, sv_blk, s, err);
+    err = "a ring-depth cap applies to the FP8 forward with d = 128 and per-tensor scales";
+    return -2;
+  }
   switch (a.d) {
     case 64:
       return sk_blk ? fp8::run<64, true>(a, vt8, sq, sk, sv, sq_blk, sk_blk, sv_blk, s, err)

@@ -9,7 +9,7 @@
 namespace ea {
 namespace fwd {
 
-template <bool kBf16, int D, int DV, int BN, bool kDrop>
+template <bool kBf16, int D, int DV, int BN, bool kDrop, bool kCap = false>
 int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   using Cfg = Config<D, DV, BN>;
   const int nk = a.nk > 0 ? a.nk : a.n;
@@ -30,7 +30,7 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
     err = "cuTensorMapEncodeTiled rejected a forward tensor map";
     return -5;
   }
-  auto kern = fwd_tc_kernel<kBf16, D, DV, BN, kDrop>;
+  auto kern = fwd_tc_kernel<kBf16, D, DV, BN, kDrop, kCap>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) {
@@ -42,6 +42,8 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
               a.lse, a.status, nsplit, nsplit > 1 ? a.o_part : nullptr,
               nsplit > 1 ? a.lse_part : nullptr, a.drop, nk, nk - a.n,
               a.n >= kRowsPerTile ? kPrefetch : 0};
+  p.ring_k = Ring::make(ring_depth(a.ring_stages, 1, Cfg::NSK));
+  p.ring_v = Ring::make(ring_depth(a.ring_stages, 1, Cfg::NSV));
   dim3 grid((a.n + 2 * kRowsPerTile - 1) / (2 * kRowsPerTile), static_cast<unsigned>(heads),
             static_cast<unsigned>(nsplit));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);
@@ -56,6 +58,14 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
 template <int D, int DV, bool kDrop>
 int launch_dd(bool bf16, const AttnArgs& a, cudaStream_t s, std::string& err) {
   const int bn = a.kv_block == 0 ? 128 : a.kv_block;
+  if (a.ring_stages != 0) {
+    // ring depths from the launch: one instantiation, as a testing aid
+    if constexpr (D == 128 && DV == 128 && !kDrop) {
+      if (bf16 && bn == 128) return run<true, 128, 128, 128, false, true>(a, s, err);
+    }
+    err = "a ring-depth cap applies to bf16, d = v = 128, key block 128, without dropout";
+    return -2;
+  }
   switch (bn) {
     case 32:
       return bf16 ? run<true, D, DV, 32, kDrop>(a, s, err) : run<false, D, DV, 32, kDrop>(a, s, err);

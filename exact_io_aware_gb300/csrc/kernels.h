@@ -12,6 +12,57 @@ namespace ea {
 
 enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskBitmap = 2 };
 
+// Depth of a shared-memory ring chosen at launch (at most the stage count the kernel's shared
+// memory holds): use i of the ring takes stage i mod n in phase parity (i / n) mod 2.  The
+// division is a multiply-high by ceil(2^32 / n), exact for every i below 2^31 when n <= 4.
+struct Ring {
+  uint32_t n;      // stages in use, 1 .. 4
+  uint32_t magic;  // ceil(2^32 / n) for n >= 2
+  static Ring make(int stages) {
+    Ring r{static_cast<uint32_t>(stages), 0u};
+    if (stages >= 2) r.magic = static_cast<uint32_t>(((uint64_t(1) << 32) + stages - 1) / stages);
+    return r;
+  }
+#ifdef __CUDACC__
+  __device__ __forceinline__ uint32_t div(int i) const {
+    return n == 1 ? static_cast<uint32_t>(i) : __umulhi(static_cast<uint32_t>(i), magic);
+  }
+  __device__ __forceinline__ int stage(int i) const {
+    return static_cast<int>(static_cast<uint32_t>(i) - div(i) * n);
+  }
+  __device__ __forceinline__ uint32_t parity(int i) const { return div(i) & 1u; }
+#endif
+};
+
+// A ring of N stages fixed at compile time (the production kernels): the same interface as
+// Ring with constant divisions.
+template <int N>
+struct StaticRing {
+#ifdef __CUDACC__
+  __device__ __forceinline__ static constexpr int stage(int i) { return i % N; }
+  __device__ __forceinline__ static constexpr uint32_t parity(int i) { return (i / N) & 1; }
+#endif
+};
+
+#ifdef __CUDACC__
+// The ring a kernel walks: the launch-time depth in the capped instantiations (kCap), else the
+// compile-time stage count.
+template <bool kCap, int N>
+__device__ __forceinline__ auto ring_of(const Ring& r) {
+  if constexpr (kCap) {
+    return r;
+  } else {
+    return StaticRing<N>{};
+  }
+}
+#endif
+
+// Stage count of a ring at launch: the caller's cap (0 = none) within [lo, hi].
+inline int ring_depth(int cap, int lo, int hi) {
+  const int want = cap > 0 ? cap : hi;
+  return want < lo ? lo : (want > hi ? hi : want);
+}
+
 // Scalar arguments of the forward kernels (tensor maps travel separately).
 struct FwdParams {
   int n;    // query rows
@@ -32,6 +83,7 @@ struct FwdParams {
   int nk;            // keys (n for square attention)
   int off;           // causal offset nk - n: query i sees keys j <= i + off
   int prefetch;      // key blocks requested into L2 ahead of the ring loads (0: none)
+  Ring ring_k, ring_v;  // depths of the K and V rings
 };
 
 // Everything a launcher needs; pointers are device pointers.
@@ -63,6 +115,7 @@ struct AttnArgs {
   float* lse_part;
   bool dropout;     // drop probabilities with the mask of dropout.cuh (p > 0)
   DropoutArgs drop;
+  int ring_stages;  // cap on the depth of every shared-memory ring (0: as deep as memory allows)
 };
 
 // Each launcher returns 0 or a negative ATTN_ERR_* code and fills `err` on failure.

@@ -343,6 +343,25 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe, without the MUFU unit: x = j + f with j the integer nearest x (adding
+// 1.5 * 2^23 rounds it away; f = x - j is exact) and f in [-1/2, 1/2]; 2^f by the degree-3
+// polynomial of least maximal relative error on that interval (Remez exchange, float32
+// coefficients, relative error below 7.5e-5: csrc/fit_exp2_poly.py), and 2^j added to the
+// exponent field.  Arguments below -125, and -inf, give 0 (ex2.approx.ftz also flushes results
+// under 2^-126); the result is exact in range up to x < 128.
+__device__ __forceinline__ float ex2_fma(float x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  const float t = x + kRound;            // j in the low mantissa bits of t
+  const float j = t - kRound;
+  const float f = x - j;
+  float p = fmaf(0.0551716685f, f, 0.242611125f);
+  p = fmaf(p, f, 0.693260968f);
+  p = fmaf(p, f, 0.999928057f);
+  // the high bits of 1.5 * 2^23 shift out of the word: only j << 23 is added
+  const int bits = __float_as_int(p) + (__float_as_int(t) << 23);
+  return x < -125.0f ? 0.0f : __int_as_float(bits);
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

@@ -364,6 +364,30 @@ int attn_device_status(void* stream);
  */
 int attn_selftest_wait_timeout(void* stream);
 
+/*
+ * Self-test of the exponential the forward kernels can compute on the FMA pipe instead of the
+ * MUFU unit (no counterpart on the pages): for the n float32 values x (device pointers),
+ * y_fma[i] = 2^x[i] by range reduction to [-1/2, 1/2] and a degree-3 relative-minimax
+ * polynomial (relative error below 7.5e-5; 0 for x < -125 and x = -inf), and
+ * y_mufu[i] = ex2.approx.ftz(x[i]).  Returns ATTN_ERR_INVALID_ARG for n < 0 or null pointers.
+ * Asynchronous on `stream`.
+ */
+int attn_selftest_exp2(const float* x, float* y_fma, float* y_mufu, int64_t n, void* stream);
+
+/*
+ * Testing aid for the kernels' pipelines (no counterpart on the pages): caps the depth of every
+ * shared-memory ring (the forward's K and V rings, the backward's query-block and K/V rings)
+ * at `stages` for the calls that follow, in every thread of the process; 0 restores the
+ * default (as many stages as shared memory holds).  A ring whose schedule needs two stages
+ * keeps two.  The depth changes only when a tile is loaded, never the arithmetic or its order,
+ * so results are bit for bit the same at every depth.  While a cap is set, only calls with
+ * bf16 inputs, d = v = 128, key block 128 (or 0) and no dropout, and the FP8 forward with
+ * d = 128 and per-tensor scales, run (one instantiation of each kernel reads its depths at
+ * launch; the others keep them constant and cost nothing); other calls return
+ * ATTN_ERR_UNSUPPORTED.  Returns ATTN_ERR_INVALID_ARG unless 0 <= stages <= 4.
+ */
+int attn_debug_set_ring_stages(int stages);
+
 /* Message describing the calling thread's most recent failed call ("" if none). */
 const char* attn_last_error(void);
 

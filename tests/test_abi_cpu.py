@@ -124,3 +124,23 @@ def test_fp8_block_entries_reject_bad_arguments_on_host(lib):
     assert fwd(sk=0) == -1                  # null scale pointer
     assert fwd(sk=274) == -3                # misaligned scale pointer
     assert fwd(o=72) == -3
+
+
+def test_ring_depth_cap_is_checked(lib):
+    assert lib.attn_debug_set_ring_stages(5) == -1
+    assert lib.attn_debug_set_ring_stages(-1) == -1
+    assert lib.attn_debug_set_ring_stages(2) == 0
+    assert lib.attn_debug_set_ring_stages(0) == 0
+
+
+def test_ring_stage_division_is_exact():
+    """The kernels' stage / parity of ring use i: a multiply-high by ceil(2^32 / n) must equal
+    i // n (n = 2, 3, 4) for every i a kernel can reach (step counts below 2^31)."""
+    import numpy as np
+    rng = np.random.default_rng(1)
+    i = np.concatenate([np.arange(0, 1 << 16), rng.integers(0, 1 << 31, 1 << 16),
+                        [(1 << 31) - 1, (1 << 31) - 2]]).astype(np.uint64)
+    for n in (2, 3, 4):
+        magic = np.uint64(((1 << 32) + n - 1) // n)
+        q = (i * magic) >> np.uint64(32)
+        assert np.array_equal(q, i // np.uint64(n)), n
