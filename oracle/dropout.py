@@ -9,15 +9,18 @@ module restates:
 
 * Mask.  For head index bh (b·H + h), query row i and key j, the generator is
   Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
-  1, 2, 3", SC 2011): counter (i, ⌊j/4⌋, bh, 0), key (seed mod 2^32, ⌊seed / 2^32⌋).  Word
-  j mod 4 of the output is compared with the integer threshold t = ⌊p·2^32 + 1/2⌋: the
-  pair (i, j) is kept iff word ≥ t.  Integer arithmetic end to end, so the mask is the same
-  bit for bit wherever it is drawn.
+  1, 2, 3", SC 2011) with counter (⌊i/4⌋, ⌊j/4⌋, bh, 0) and key (seed mod 2^32,
+  ⌊seed / 2^32⌋): one call decides the 4 x 4 patch of pairs with those row and key groups.
+  Word i mod 4 of its output belongs to row i, and byte j mod 4 of that word (bits
+  8 (j mod 4) .. 8 (j mod 4) + 7) to key j; the pair is kept iff that byte ≥ t, the 8-bit
+  threshold t = ⌊p·256 + 1/2⌋.  The drop probability is therefore p' = t / 256 (p rounded to
+  a multiple of 1/256), and kept probabilities are scaled by 1/(1 − p').  Integer arithmetic
+  end to end, so the mask is the same bit for bit wherever it is drawn.
 * Forward.  P_ij = exp(s_ij − LSE_i) as without dropout (LSE is not changed by dropout);
-  O_i = Σ_j P_ij M_ij V_j / (1 − p).
-* Reverse, for upstream G: with P̃ = P∘M/(1 − p), dV = P̃ᵀ G;  dP̃_ij = G_i·V_j;
-  D_i = G_i·O_i (= Σ_j P̃_ij dP̃_ij);  dS_ij = P_ij (M_ij dP̃_ij/(1 − p) − D_i);
-  dQ = c·dS K, dK = c·dSᵀ Q.  This is the chain rule through O = (P∘M/(1−p)) V and the
+  O_i = Σ_j P_ij M_ij V_j / (1 − p').
+* Reverse, for upstream G: with P̃ = P∘M/(1 − p'), dV = P̃ᵀ G;  dP̃_ij = G_i·V_j;
+  D_i = G_i·O_i (= Σ_j P̃_ij dP̃_ij);  dS_ij = P_ij (M_ij dP̃_ij/(1 − p') − D_i);
+  dQ = c·dS K, dK = c·dSᵀ Q.  This is the chain rule through O = (P∘M/(1−p')) V and the
   softmax, the mask held fixed.
 """
 from __future__ import annotations
@@ -50,21 +53,34 @@ def philox4x32(ctr, key, rounds=10):
 
 
 def threshold(p):
-    """Integer drop threshold ⌊p·2^32 + 1/2⌋ (halves round up) for 0 <= p < 1."""
+    """8-bit drop threshold ⌊p·256 + 1/2⌋ (halves round up); p must leave some pairs kept
+    (threshold at most 255)."""
     if not 0.0 <= p < 1.0:
         raise ValueError("drop probability must be in [0, 1)")
-    return int(math.floor(p * 2.0 ** 32 + 0.5))
+    t = int(math.floor(p * 256.0 + 0.5))
+    if t > 255:
+        raise ValueError("drop probability rounds to 1 at 1/256 resolution")
+    return t
+
+
+def effective_p(p):
+    """The drop probability the mask realises: the threshold over 256."""
+    return threshold(p) / 256.0
 
 
 def keep_mask(seed, bh, rows, n, p):
     """Kept pairs of head ``bh`` for query ``rows`` and keys 0..n-1: bool [len(rows), n]."""
     rows = np.asarray(rows, dtype=np.int64)
-    ctr = np.zeros((rows.size, (n + 3) // 4, 4), dtype=np.uint64)
-    ctr[..., 0] = rows[:, None]
-    ctr[..., 1] = np.arange((n + 3) // 4)[None, :]
+    groups = (n + 3) // 4
+    ctr = np.zeros((rows.size, groups, 4), dtype=np.uint64)
+    ctr[..., 0] = (rows // 4)[:, None]
+    ctr[..., 1] = np.arange(groups)[None, :]
     ctr[..., 2] = bh
-    words = philox4x32(ctr, (seed & _MASK32, (seed >> 32) & _MASK32)).reshape(rows.size, -1)[:, :n]
-    return words.astype(np.uint64) >= np.uint64(threshold(p))
+    words = philox4x32(ctr, (seed & _MASK32, (seed >> 32) & _MASK32))  # [rows, groups, 4]
+    mine = np.take_along_axis(words, (rows % 4)[:, None, None].repeat(groups, axis=1), axis=2)[..., 0]
+    j = np.arange(n)
+    byte = (mine[:, j // 4].astype(np.uint64) >> (8 * (j % 4)).astype(np.uint64)) & np.uint64(0xFF)
+    return byte >= np.uint64(threshold(p))
 
 
 def forward_rows(q, k, v, c, allowed, keep, p):
@@ -77,7 +93,7 @@ def forward_rows(q, k, v, c, allowed, keep, p):
     ell = e.sum(axis=1)
     safe = np.where(nonempty, ell, 1.0)
     P = e / safe[:, None]
-    y = ((P * keep) @ v) / (1.0 - p)
+    y = ((P * keep) @ v) / (1.0 - effective_p(p))
     y[~nonempty] = 0.0
     lse = np.where(nonempty, m + np.log(safe), -np.inf)
     return y, lse
@@ -90,11 +106,12 @@ def backward_head(q, k, v, c, allowed, keep, p, G):
     s = np.where(allowed, float(c) * (q @ k.T), -np.inf)
     fin = np.isfinite(lse)
     P = np.where(fin[:, None], np.exp(s - np.where(fin, lse, 0.0)[:, None]), 0.0)
-    Pt = P * keep / (1.0 - p)
+    pe = effective_p(p)
+    Pt = P * keep / (1.0 - pe)
     dV = Pt.T @ G
     dPt = G @ v.T
     D = (G * y).sum(axis=1)
-    dS = P * (keep * dPt / (1.0 - p) - D[:, None])
+    dS = P * (keep * dPt / (1.0 - pe) - D[:, None])
     dQ = float(c) * dS @ k
     dK = float(c) * dS.T @ q
     return dQ, dK, dV

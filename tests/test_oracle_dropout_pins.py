@@ -38,24 +38,43 @@ def test_philox_rounds_matter():
 @pytest.mark.parametrize("p", [0.1, 0.3, 0.5])
 def test_keep_rate_and_independence(p):
     keep = dropout.keep_mask(0x1234_5678_9ABC, 3, np.arange(300), 1000, p)
+    pe = dropout.effective_p(p)
     n = keep.size
-    sd = math.sqrt(p * (1 - p) / n)
-    assert abs(keep.mean() - (1 - p)) < 5 * sd
-    # neighbouring keys, which share one generator call, are not correlated
-    a, b = keep[:, 0::4].ravel(), keep[:, 1::4].ravel()
-    assert abs(np.mean(a & b) - (1 - p) ** 2) < 5 * math.sqrt((1 - p) ** 2 / a.size)
+    sd = math.sqrt(pe * (1 - pe) / n)
+    assert abs(keep.mean() - (1 - pe)) < 5 * sd
+    # pairs one generator call decides together are not correlated: neighbouring keys of a
+    # row and neighbouring rows of a key
+    for a, b in ((keep[:, 0::4], keep[:, 1::4]), (keep[0::4, :], keep[1::4, :])):
+        a, b = a.ravel(), b.ravel()
+        assert abs(np.mean(a & b) - (1 - pe) ** 2) < 5 * math.sqrt((1 - pe) ** 2 / a.size)
     # different seeds or heads give different masks
     other = dropout.keep_mask(0x1234_5678_9ABD, 3, np.arange(300), 1000, p)
-    assert np.mean(other != keep) > 0.5 * 2 * p * (1 - p)
+    assert np.mean(other != keep) > 0.5 * 2 * pe * (1 - pe)
     assert np.any(dropout.keep_mask(0x1234_5678_9ABC, 4, np.arange(300), 1000, p) != keep)
 
 
 def test_threshold_edges():
     assert dropout.threshold(0.0) == 0
-    assert dropout.threshold(0.5) == 2 ** 31
-    with pytest.raises(ValueError):
-        dropout.threshold(1.0)
+    assert dropout.threshold(0.5) == 128
+    assert dropout.threshold(0.1) == 26 and dropout.effective_p(0.1) == 26 / 256
+    assert dropout.threshold(0.998) == 255
+    for bad in (0.999, 1.0, -0.1):
+        with pytest.raises(ValueError):
+            dropout.threshold(bad)
     assert dropout.keep_mask(7, 0, np.arange(5), 9, 0.0).all()
+
+
+@pytest.mark.parametrize("p", [0.25, 0.5, 0.9])
+def test_patch_layout_from_the_published_vector(p):
+    """Rows 0-3 x keys 0-3 of head 0 under seed 0 are one generator call: counter (0,0,0,0),
+    key (0,0), the first published known-answer vector.  Row x reads word x, key y byte y
+    (least significant first); the pair is kept iff the byte reaches the 8-bit threshold."""
+    ctr, key, out = _kat()[0]
+    assert ctr == (0, 0, 0, 0) and key == (0, 0)
+    t = int(math.floor(p * 256 + 0.5))
+    want = [[((out[x] >> (8 * y)) & 0xFF) >= t for y in range(4)] for x in range(4)]
+    got = dropout.keep_mask(0, 0, np.arange(4), 4, p)
+    assert got.tolist() == want
 
 
 def test_zero_probability_is_plain_attention():
