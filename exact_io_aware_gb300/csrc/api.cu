@@ -221,13 +221,16 @@ extern "C" {
 
 namespace {
 
-// Dropout arguments of a call: p in [0, 1); threshold floor(p 2^32 + 1/2), scale 1/(1-p).
+// Dropout arguments of a call: p in [0, 1); 8-bit threshold t = floor(p 256 + 1/2) <= 255
+// (the drop probability realised is t / 256), scale 256 / (256 - t).
 int set_dropout(float p_drop, uint64_t seed, ea::AttnArgs& a) {
   if (!(p_drop >= 0.0f && p_drop < 1.0f))
     return fail(ATTN_ERR_INVALID_ARG, "p_drop must lie in [0, 1)");
+  const int t = static_cast<int>(std::floor(static_cast<double>(p_drop) * 256.0 + 0.5));
+  if (t > 255) return fail(ATTN_ERR_INVALID_ARG, "p_drop rounds to 1 at the mask's 1/256 resolution");
   a.dropout = p_drop > 0.0f;
-  a.drop.thr = static_cast<uint32_t>(std::floor(static_cast<double>(p_drop) * 4294967296.0 + 0.5));
-  a.drop.scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  a.drop.thr4 = static_cast<uint32_t>(t) * 0x01010101u;
+  a.drop.scale = static_cast<float>(256.0 / (256.0 - t));
   a.drop.seed_lo = static_cast<uint32_t>(seed);
   a.drop.seed_hi = static_cast<uint32_t>(seed >> 32);
   return ATTN_OK;

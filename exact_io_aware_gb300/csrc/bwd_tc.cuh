@@ -436,28 +436,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // Dropout: keep bits of this key with the warp's query columns (bit k of word h <->
       // query q0 + c_lo + 32 h + k), drawn while the scores are still being computed.  One
-      // generator call covers four consecutive keys of one query, and the four lanes of a key
-      // group (4 | key0 + 32 quad) share those keys: lane l draws the calls of queries
-      // 4g + (l & 3), g = 0..7, and the group swaps the 4-bit results with four shuffles.
+      // generator call decides a 4 x 4 patch of (query, key) pairs; the four lanes of a key
+      // group (keys 4 g .. 4 g + 3, lanes 4 a .. 4 a + 3) share its calls: lane s draws the
+      // patches of queries q0 + c_lo + 16 s .. + 15 and the group exchanges the columns.
       uint32_t kbits[kDrop ? kHalf / 32 : 1];
       if constexpr (kDrop) {
-        const uint32_t sub = static_cast<uint32_t>(lane & 3);
+        uint32_t part[4];
+        keep_cols<kHalf / 16>(p.drop, static_cast<uint32_t>(q0 + c_lo) >> 2,
+                              static_cast<uint32_t>(j) >> 2, bh, part);
 #pragma unroll
-        for (int h = 0; h < kHalf / 32; ++h) {
-          uint32_t mine = 0;  // nibble g: keep bits of keys 4 (j / 4) .. +3 with query 4g + sub
-#pragma unroll 1
-          for (int g = 0; g < 8; ++g)
-            mine |= keep4(p.drop, static_cast<uint32_t>(q0 + c_lo + 32 * h + 4 * g) + sub,
-                          static_cast<uint32_t>(j) >> 2, bh) << (4 * g);
-          uint32_t w = 0;
+        for (int h = 0; h < kHalf / 32; ++h) kbits[h] = 0u;
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const uint32_t got = __shfl_sync(0xFFFFFFFFu, mine, (lane & ~3) | t);
-#pragma unroll
-            for (int g = 0; g < 8; ++g) w |= ((got >> (4 * g + sub)) & 1u) << (4 * g + t);
-          }
-          kbits[h] = w;
-        }
+        for (int s = 0; s < 4; ++s) kbits[(s * kHalf / 4) / 32] |= part[s] << ((s * kHalf / 4) % 32);
       }
       ok = mbar_wait_spin(&bars.s_full, i & 1, p.status, 27);
       if (!ok) break;

@@ -484,15 +484,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // key0 + c_lo + 32 h + k), drawn before the wait for dP.
       uint32_t kbits[kDrop ? kHalf / 32 : 1];
       if constexpr (kDrop) {
+        // one generator call per 4 x 4 patch: lane s of each group of four (rows 4 r ..) draws
+        // the patches of keys key0 + c_lo + 16 s .. + 15
+        uint32_t part[4];
+        keep_rows<kHalf / 16>(p.drop, static_cast<uint32_t>(row) >> 2,
+                              static_cast<uint32_t>(key0 + c_lo) >> 2, bh, part);
 #pragma unroll
-        for (int h = 0; h < kHalf / 32; ++h) {
-          uint32_t w = 0;
-#pragma unroll 1
-          for (int g = 0; g < 8; ++g)
-            w |= keep4(p.drop, static_cast<uint32_t>(row),
-                       static_cast<uint32_t>(key0 + c_lo + 32 * h + 4 * g) >> 2, bh) << (4 * g);
-          kbits[h] = w;
-        }
+        for (int h = 0; h < kHalf / 32; ++h) kbits[h] = 0u;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) kbits[(s * kHalf / 4) / 32] |= part[s] << ((s * kHalf / 4) % 32);
       }
       ok = mbar_wait_spin(&bars.dp_full, i & 1, p.status, 48);
       if (!ok) break;

@@ -461,15 +461,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // while the scores are still being computed; the exponential loop only tests them.
       uint32_t kbits[kDrop ? BN / 32 : 1];
       if constexpr (kDrop) {
+        // rows 4 r .. 4 r + 3 are lanes 4 a .. 4 a + 3 (the warp's rows start at a multiple of
+        // 32); lane s of such a group draws the generator calls of keys key0 + s BN / 4 ..
+        uint32_t part[4];
+        keep_rows<BN / 16>(p.drop, static_cast<uint32_t>(row) >> 2,
+                           static_cast<uint32_t>(key0) >> 2, bh, part);
 #pragma unroll
-        for (int q = 0; q < BN / 32; ++q) {
-          uint32_t w = 0;
-#pragma unroll 1
-          for (int g = 0; g < 8; ++g)
-            w |= keep4(p.drop, static_cast<uint32_t>(row),
-                       static_cast<uint32_t>(key0 + 32 * q + 4 * g) >> 2, bh) << (4 * g);
-          kbits[q] = w;
-        }
+        for (int q = 0; q < BN / 32; ++q) kbits[q] = 0u;
+#pragma unroll
+        for (int s = 0; s < 4; ++s) kbits[(s * BN / 4) / 32] |= part[s] << ((s * BN / 4) % 32);
       }
       ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
       if (!ok) break;

@@ -100,13 +100,17 @@ int attn_fwd(int dtype, int B, int H, int n, int d, float c,
  * dropout and ask of any dropout extension that its reverse pass replay the realised mask
  * ("Exact tiled attention and memory-aware differentiation", reverse procedure; closing
  * remark).  Here the mask is a pure function of (seed, head, query row, key), so the forward
- * and attn_bwd_dropout draw the same mask and no mask is stored:
- *   words = Philox4x32-10(counter = (i, floor(j / 4), b * H + h, 0), key = (seed mod 2^32,
- *           floor(seed / 2^32)))  (Salmon et al., "Parallel random numbers: as easy as 1, 2,
- *           3", SC 2011); the pair (i, j) is kept iff words[j mod 4] >= floor(p_drop 2^32 + 1/2).
- *   O_i = sum_j P_ij keep_ij V_j / (1 - p_drop), P = softmax as without dropout.
- * LSE is that of the undropped scores (the statistic the backward needs).
- *   p_drop  drop probability, 0 <= p_drop < 1 (0 gives exactly attn_fwd's result)
+ * and attn_bwd_dropout draw the same mask and no mask is stored.  One generator call decides a
+ * 4 x 4 patch of (query, key) pairs:
+ *   words = Philox4x32-10(counter = (floor(i / 4), floor(j / 4), b * H + h, 0),
+ *           key = (seed mod 2^32, floor(seed / 2^32)))  (Salmon et al., "Parallel random
+ *           numbers: as easy as 1, 2, 3", SC 2011); the pair (i, j) is kept iff byte j mod 4
+ *           (least significant first) of words[i mod 4] >= t, t = floor(p_drop 256 + 1/2).
+ *   O_i = sum_j P_ij keep_ij V_j / (1 - p'), p' = t / 256, P = softmax as without dropout.
+ * The drop probability is thus p_drop rounded to a multiple of 1/256.  LSE is that of the
+ * undropped scores (the statistic the backward needs).
+ *   p_drop  drop probability, 0 <= p_drop < 1 and t <= 255 (0 gives exactly attn_fwd's result);
+ *           ATTN_ERR_INVALID_ARG otherwise
  *   seed    64-bit generator key; the same (seed, p_drop) must be passed to attn_bwd_dropout
  * Other arguments, outputs and errors as for attn_fwd.
  */
@@ -281,8 +285,9 @@ int attn_bwd(int dtype, int B, int H, int n, int d, float c,
 
 /*
  * Backward pass of attn_fwd_dropout, replaying the same mask (same seed and p_drop).  With
- * P~ = P * keep / (1 - p_drop): dV = P~^T dO;  D_i = dO_i . O_i (O the dropped output);
- * dS_ij = P_ij (keep_ij (dO_i . V_j) / (1 - p_drop) - D_i);  dQ = c dS K,  dK = c dS^T Q.
+ * p' = floor(p_drop 256 + 1/2) / 256 and P~ = P * keep / (1 - p'): dV = P~^T dO;
+ * D_i = dO_i . O_i (O the dropped output);  dS_ij = P_ij (keep_ij (dO_i . V_j) / (1 - p') - D_i);
+ * dQ = c dS K,  dK = c dS^T Q.
  * Other arguments, outputs, workspace and errors as for attn_bwd.
  */
 int attn_bwd_dropout(int dtype, int B, int H, int n, int d, float c,

@@ -99,6 +99,20 @@ def forward_rows(q, k, v, c, allowed, keep, p):
     return y, lse
 
 
+def probabilities_and_gamma(q, k, v, c, allowed, keep, p, G):
+    """P [n,n] (undropped probabilities), dP̃ = G Vᵀ [n,n] and γ = dS [n,n] of one head under
+    dropout with kept pairs ``keep``: γ_ij = P_ij (M_ij dP̃_ij/(1 − p') − D_i)."""
+    q, k, v, G = (np.asarray(x, dtype=np.float64) for x in (q, k, v, G))
+    y, lse = forward_rows(q, k, v, c, allowed, keep, p)
+    s = np.where(allowed, float(c) * (q @ k.T), -np.inf)
+    fin = np.isfinite(lse)
+    P = np.where(fin[:, None], np.exp(s - np.where(fin, lse, 0.0)[:, None]), 0.0)
+    dPt = G @ v.T
+    D = (G * y).sum(axis=1)
+    gamma = P * (keep * dPt / (1.0 - effective_p(p)) - D[:, None])
+    return P, dPt, gamma
+
+
 def backward_head(q, k, v, c, allowed, keep, p, G):
     """dQ, dK, dV of one head under dropout (the mask ``keep`` replayed)."""
     q, k, v, G = (np.asarray(x, dtype=np.float64) for x in (q, k, v, G))

@@ -29,10 +29,12 @@ def _window_bits(n, lo, width):
     return allowed, torch.from_numpy(pack_bitmap(allowed).view(np.int32)).cuda()
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("dtype,kvb", [("bf16", 128), ("bf16", 64), ("bf16", 32), ("f16", 0),
+                                       ("f32", 0)])
 @pytest.mark.parametrize("p", [0.3, 0.75])
-def test_forward_mask_is_bit_exact(dtype, p):
-    """c = 0 and a 128-key window J0.. per row: O[i, a] = keep(i, J0 + a) / (128 (1 - p))."""
+def test_forward_mask_is_bit_exact(dtype, kvb, p):
+    """c = 0 and a 128-key window J0.. per row: O[i, a] = keep(i, J0 + a) / (128 (1 - p')), p' the
+    drop probability at the mask's 1/256 resolution."""
     B, H, n, d, j0 = 1, 3, 1000, 128, 640
     allowed, bits = _window_bits(n, j0, d)
     v = torch.zeros((B, H, n, d), dtype=TORCH_DTYPE[dtype], device="cuda")
@@ -40,20 +42,22 @@ def test_forward_mask_is_bit_exact(dtype, p):
     q = torch.randn((B, H, n, d), device="cuda").to(v.dtype)
     k = torch.randn((B, H, n, d), device="cuda").to(v.dtype)
     p32 = float(np.float32(p))
-    o, lse = ea.attn_fwd(q, k, v, 0.0, mask="bitmap", mask_bits=bits, dropout_p=p32, seed=SEED)
+    o, lse = ea.attn_fwd(q, k, v, 0.0, mask="bitmap", mask_bits=bits, dropout_p=p32, seed=SEED,
+                         kv_block=kvb)
     assert ea.attn_device_status() == ea.ATTN_OK
     got = (o.float().cpu().numpy() != 0)
     for bh in range(B * H):
         want = odrop.keep_mask(SEED, bh, np.arange(n), n, p32)[:, j0:j0 + d]
         assert np.array_equal(got[bh // H, bh % H], want), f"head {bh}"
     nz = o.float()[o != 0]
-    assert torch.allclose(nz, torch.full_like(nz, 1.0 / (d * (1.0 - p32))), rtol=1e-2)
+    pe = odrop.effective_p(p32)
+    assert torch.allclose(nz, torch.full_like(nz, 1.0 / (d * (1.0 - pe))), rtol=1e-2)
     assert torch.allclose(lse, torch.full_like(lse, float(np.log(d))), atol=1e-5)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_backward_mask_is_bit_exact(dtype):
-    """c = 0, n = d = 128, dO_i = e_i: dV[j, a] = keep(a, j) / (128 (1 - p))."""
+    """c = 0, n = d = 128, dO_i = e_i: dV[j, a] = keep(a, j) / (128 (1 - p'))."""
     B, H, n, d, p = 1, 2, 128, 128, 0.4
     p32 = float(np.float32(p))
     dt = TORCH_DTYPE[dtype]
@@ -137,6 +141,10 @@ def test_zero_probability_and_determinism():
                               ea._ptr(dev["v"]), 0, None, 0, 0, 0, 1.0, 1, ea._ptr(oz),
                               ea._ptr(lz), None)
     assert rc == ea.ATTN_ERR_INVALID_ARG  # p_drop = 1 is refused
+    rc = lib.attn_fwd_dropout(2, 1, 1, 16, 64, 0.1, ea._ptr(dev["q"]), ea._ptr(dev["k"]),
+                              ea._ptr(dev["v"]), 0, None, 0, 0, 0, 0.999, 1, ea._ptr(oz),
+                              ea._ptr(lz), None)
+    assert rc == ea.ATTN_ERR_INVALID_ARG  # rounds to 1 at the mask's 1/256 resolution
 
 
 def test_autograd_wrapper_with_dropout():
@@ -151,3 +159,40 @@ def test_autograd_wrapper_with_dropout():
     check_forward(y.detach(), torch.from_numpy(L), Y, L, "bf16", "autograd")
     for got, want in zip((q.grad, k.grad, v.grad), grads):
         assert rel_frob_per_head(got, want).max() <= tol_grad("bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_dq_kernel_mask_is_bit_exact(dtype):
+    """The query-tile kernel's mask, read out of dQ: with the keys one-hot in a 128-key window,
+    dQ[i, b] = c γ_{i, j0+b} is a single product, and a kept or dropped pair changes it by
+    c P_ij dP_ij / (1 - p').  Every element must lie nearer the value its mask bit gives than the
+    value the flipped bit would give (where the two differ by more than rounding)."""
+    B, H, n, d, p = 1, 1, 300, 128, 0.4
+    j0 = 128
+    p32 = float(np.float32(p))
+    pe = odrop.effective_p(p32)
+    wl = Workload("dropout_dq", 55, B, H, n, d, dtype, "causal", d ** -0.5)
+    inp = head_inputs(wl)
+    kk = np.zeros((B, H, n, d), np.float32)
+    kk[0, 0, j0:j0 + d] = np.eye(d, dtype=np.float32)
+    inp["k"] = kk
+    dev = {t: to_dev(inp[t], dtype) for t in inp}
+    o, lse = ea.attn_fwd(dev["q"], dev["k"], dev["v"], wl.c, mask="causal", dropout_p=p32,
+                         seed=SEED)
+    dq, _, _ = ea.attn_bwd(dev["q"], dev["k"], dev["v"], o, lse, dev["do"], wl.c, mask="causal",
+                           dropout_p=p32, seed=SEED)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    rows = np.arange(n)
+    a = np.tril(np.ones((n, n), bool))
+    keep = odrop.keep_mask(SEED, 0, rows, n, p32)
+    P, dPt, gamma = odrop.probabilities_and_gamma(*(inp[t][0, 0] for t in ("q", "k", "v")), wl.c,
+                                                  a, keep, p32, inp["do"][0, 0])
+    keys = np.arange(j0, j0 + d)
+    want = wl.c * gamma[:, keys]
+    flip = wl.c * (gamma + P * dPt / (1.0 - pe) * (1 - 2 * keep))[:, keys]
+    got = dq[0, 0].double().cpu().numpy()
+    sep = np.abs(want - flip) > 1e-2 * (np.abs(want) + np.abs(flip)) + 1e-6
+    assert sep.sum() > 0.5 * a[:, keys].sum()
+    nearer = np.abs(got - want) < np.abs(got - flip)
+    bad = sep & ~nearer
+    assert not bad.any(), f"mask bit wrong at {np.argwhere(bad)[:5].tolist()}"

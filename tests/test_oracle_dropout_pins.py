@@ -137,3 +137,16 @@ def test_dropout_key_gradient_sums_to_zero_and_output_is_unbiased():
         acc += dropout.forward_rows(q, k, v, 0.5, a, dropout.keep_mask(s, 0, np.arange(n), n, p),
                                     p)[0]
     assert np.max(np.abs(acc / seeds - y0)) < 0.1
+
+
+def test_gamma_pieces_agree_with_the_reverse_pass():
+    rng = np.random.default_rng(6)
+    n, d, p, c = 12, 4, 0.35, 0.7
+    q, k, v, g = (rng.normal(size=(n, d)) for _ in range(4))
+    a = masks.causal(n)(0, np.arange(n))
+    keep = dropout.keep_mask(3, 1, np.arange(n), n, p)
+    P, dPt, gamma = dropout.probabilities_and_gamma(q, k, v, c, a, keep, p, g)
+    dQ, dK, _ = dropout.backward_head(q, k, v, c, a, keep, p, g)
+    assert np.max(np.abs(c * gamma @ k - dQ)) < 1e-12
+    assert np.max(np.abs(c * gamma.T @ q - dK)) < 1e-12
+    assert np.array_equal(P[~a], np.zeros(np.count_nonzero(~a)))
