@@ -181,6 +181,7 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.num_splits = 1;
   a.nk = n;
   a.ring_stages = g_ring_stages.load(std::memory_order_relaxed);
+  a.fwd_rows_cta = 256;
   return a;
 }
 
@@ -259,6 +260,13 @@ int fwd_general(int dtype, int B, int H, int nq, int nk, int d, int v_dim, float
   a.o_out = o;
   a.lse = lse;
   if (int rc = set_dropout(p_drop, seed, a)) return rc;
+  // One 128-row tile per CTA when two-tile CTAs would fill at most half the multiprocessors:
+  // twice the CTAs then run at once, and each finishes its tile sooner than a pair.
+  if (splits == 1 && dtype != ATTN_F32) {
+    const int64_t ctas = static_cast<int64_t>((nq + 255) / 256) * B * H;
+    const int sms = sm_count();
+    if (sms > 0 && 2 * ctas <= sms) a.fwd_rows_cta = 128;
+  }
   if (splits > 1) {
     const size_t need = split_ws_bytes(B, H, nq, v_dim, splits);
     if (!workspace || workspace_bytes < need)

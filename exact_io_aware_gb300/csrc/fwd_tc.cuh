@@ -135,9 +135,9 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 }
 
 // Step word of the walk under no mask or the causal mask: key block j, and for each of the two
-// query tiles (rows r0 .. r0 + 127 of the pair) whether it skips the block, takes it whole or
-// needs the mask pass (causal diagonal or the ragged key tail).  Same encoding as the bitmap
-// table: j | cls0 << 16 | cls1 << 18.
+// query tiles (rows r0 .. r0 + 127 of the pair; rows from n on do not exist) whether it skips
+// the block, takes it whole or needs the mask pass (causal diagonal or the ragged key tail).
+// Same encoding as the bitmap table: j | cls0 << 16 | cls1 << 18.
 __device__ __forceinline__ uint32_t dense_step(int j, int BN, int nblk, int n, int nk, int off,
                                                int pair_row0, bool causal) {
   uint32_t w = static_cast<uint32_t>(j);
@@ -187,7 +187,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int off = p.off;
   const int bh = blockIdx.y;
   const int pair = (gridDim.x - 1 - blockIdx.x);  // heaviest (causal) query tiles first
-  const int pair_row0 = pair * 2 * kRowsPerTile;  // tile t starts at pair_row0 + 128 t
+  // tile t starts at pair_row0 + 128 t; with p.rows_cta = 128 (grids that would fill at most half
+  // the multiprocessors) a CTA owns one tile and tile 1 has no rows
+  const int pair_row0 = pair * p.rows_cta;
+  const int nrow = min(n, pair_row0 + p.rows_cta);  // end of this CTA's rows
   const int nblk = (nk + BN - 1) / BN;
   const int split = blockIdx.z;
   const int nsplit = gridDim.z;
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // otherwise step i is block j_lo + i, up to the last block of the share.
   const bool use_table = p.mask_kind == kMaskBitmap;
   const bool causal = p.mask_kind == kMaskCausal;
-  const int pair_last = min(pair_row0 + 2 * kRowsPerTile, n) - 1;  // last row of the pair
+  const int pair_last = nrow - 1;  // last row of the CTA
   const int last_key = pair_last + off;  // causal: the last key the pair's rows see
   const int reach = use_table ? nblk : (causal ? (last_key < 0 ? 0 : last_key / BN + 1) : nblk);
   const int share = (reach + nsplit - 1) / nsplit;
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < kSoftmaxThreads) {
       const int t = tid / kRowsPerTile;
       const int row = pair_row0 + t * kRowsPerTile + (tid % kRowsPerTile);
-      const bool valid = row < n;
+      const bool valid = row < nrow;
       const uint32_t* rowbits =
           p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
           static_cast<int64_t>(valid ? row : 0) * p.mask_row_words;
@@ -274,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t act = 0;
     for (int t = 0; t < 2; ++t) {
       const int r0 = pair_row0 + t * kRowsPerTile;
-      if (r0 >= n || j_lo >= j_hi) continue;
-      const int tile_last_key = min(r0 + kRowsPerTile, n) - 1 + off;
+      if (r0 >= nrow || j_lo >= j_hi) continue;
+      const int tile_last_key = min(r0 + kRowsPerTile, nrow) - 1 + off;
       if (causal && tile_last_key < 0) continue;  // no row of the tile sees a key
       const int last_blk = causal ? tile_last_key / BN : nblk - 1;
       if (j_lo <= last_blk) act |= 1u << t;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t act = bars.act;
   // tensor memory: S_t at tmem + t*BN, O_t at tmem + 2*BN + t*DV
   auto step_at = [&](int i) -> uint32_t {
-    return use_table ? steps[i] : dense_step(j_lo + i, BN, nblk, n, nk, off, pair_row0, causal);
+    return use_table ? steps[i] : dense_step(j_lo + i, BN, nblk, nrow, nk, off, pair_row0, causal);
   };
 
   if (warp == kProducerWarp) {
@@ -450,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t* rowbits =
         p.mask_kind == kMaskBitmap
             ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
-                  static_cast<int64_t>(row < n ? row : 0) * p.mask_row_words
+                  static_cast<int64_t>(row < nrow ? row : 0) * p.mask_row_words
             : nullptr;
     for (int i = 0; i < nsteps && ok; ++i) {
       const uint32_t sw = step_at(i);
@@ -485,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kq = key0 + q * 32;
           uint32_t w;
           if (p.mask_kind == kMaskBitmap) {
-            w = (row < n && kq < nk) ? __ldg(rowbits + kq / 32) : 0u;
+            w = (row < nrow && kq < nk) ? __ldg(rowbits + kq / 32) : 0u;
             const int left = nk - kq;
             if (left < 32) w &= left > 0 ? (1u << left) - 1u : 0u;
           } else {
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (partial_out) {
       // Key split: this share's normalised partial, float32, one row per thread.  A row with
       // no allowed key in the share gets O_z = 0 and LSE_z = -inf (not an empty row overall).
-      if (pair_row0 + t * kRowsPerTile < n) {
+      if (pair_row0 + t * kRowsPerTile < nrow) {
         if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
         tc_fence_after();
         const float inv = l > 0.0f ? (kDrop ? p.drop.scale : 1.0f) / l : 0.0f;
@@ -619,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int k = 0; k < 16; ++k) rr[k] = 0u;
             }
-            if (row < n) {
+            if (row < nrow) {
 #pragma unroll
               for (int k = 0; k < 16; k += 4)
                 dst[(c0 + k) / 4] =
@@ -627,11 +630,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 __uint_as_float(rr[k + 2]) * inv, __uint_as_float(rr[k + 3]) * inv);
             }
           }
-          if (row < n)
+          if (row < nrow)
             p.lse_part[prow] = l > 0.0f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
         }
       }
-    } else if (pair_row0 + t * kRowsPerTile < n) {
+    } else if (pair_row0 + t * kRowsPerTile < nrow) {
       // A tile with rows but no allowed key at all (possible only under a bitmap) writes zeros
       // and -inf, like any other row with an empty allowed set.
       if (active && ok) ok = mbar_wait(&bars.o_done[t], 0, p.status, 9);
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(stage + TO::offset(r, c0 + 8)) =
               make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
-        if (row < n) {
+        if (row < nrow) {
           p.lse[static_cast<int64_t>(bh) * n + row] =
               l > 0.0f ? (m + __log2f(l)) * 0.6931471805599453f : -INFINITY;
           if (!(l > 0.0f)) raise_empty_row(p.status);

@@ -84,6 +84,7 @@ struct FwdParams {
   int off;           // causal offset nk - n: query i sees keys j <= i + off
   int prefetch;      // key blocks requested into L2 ahead of the ring loads (0: none)
   Ring ring_k, ring_v;  // depths of the K and V rings
+  int rows_cta;      // query rows per CTA: 256 (two tiles), or 128 when a grid is small
 };
 
 // Everything a launcher needs; pointers are device pointers.
@@ -116,6 +117,7 @@ struct AttnArgs {
   bool dropout;     // drop probabilities with the mask of dropout.cuh (p > 0)
   DropoutArgs drop;
   int ring_stages;  // cap on the depth of every shared-memory ring (0: as deep as memory allows)
+  int fwd_rows_cta;  // forward: query rows per CTA (256, or 128 for grids under half the SMs)
 };
 
 // Each launcher returns 0 or a negative ATTN_ERR_* code and fills `err` on failure.

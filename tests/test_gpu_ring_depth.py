@@ -47,13 +47,15 @@ def _run_all(dev, c, mask, bits, kvb, drop):
     return (o, lse) + tuple(grads)
 
 
-@pytest.mark.parametrize("mask,n,kvb", [
-    ("none", 700, 128), ("causal", 1100, 0), ("bitmap", 513, 128), ("causal", 4096, 0),
-    ("none", 128, 0), ("bitmap", 1, 128),
+@pytest.mark.parametrize("mask,n,kvb,H", [
+    ("none", 700, 128, 3), ("causal", 1100, 0, 3), ("bitmap", 513, 128, 3), ("causal", 4096, 0, 3),
+    ("none", 128, 0, 3), ("bitmap", 1, 128, 3),
+    # enough heads that the forward keeps two query tiles per CTA (grid over half the SMs)
+    ("causal", 2048, 0, 10),
 ])
-def test_outputs_do_not_depend_on_ring_depth(mask, n, kvb):
+def test_outputs_do_not_depend_on_ring_depth(mask, n, kvb, H):
     d = 128
-    wl = Workload("ring", 17, 1, 3, n, d, "bf16", mask, d ** -0.5)
+    wl = Workload("ring", 17, 1, H, n, d, "bf16", mask, d ** -0.5)
     inp = head_inputs(wl)
     dev = {t: to_dev(inp[t], "bf16") for t in inp}
     bits = _bits(mask, n)
