@@ -182,6 +182,7 @@ ea::AttnArgs make_args(int B, int H, int n, int d, float c, const void* q, const
   a.nk = n;
   a.ring_stages = g_ring_stages.load(std::memory_order_relaxed);
   a.fwd_rows_cta = 256;
+  a.sms = sm_count();
   return a;
 }
 

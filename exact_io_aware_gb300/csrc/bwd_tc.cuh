@@ -71,6 +71,8 @@ struct BwdParams {
   DropoutArgs drop;  // read only by the dropout instantiations
   Ring ring_q;          // depth of the dK/dV kernel's (Q, dO, row table) ring
   Ring ring_k, ring_v;  // depths of the dQ kernel's K and V rings
+  int next_cta;         // CTAs resident at once (the SM count): the CTA launched that many after
+                        // this one has its first tiles requested into L2 (0: none)
 };
 
 __host__ __device__ constexpr int pad32(int x) { return x < 32 ? 32 : x; }
@@ -285,6 +287,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_g);
+      // The CTA launched p.next_cta after this one (one per SM, in launch order) finds its K and
+      // V tiles and its first query block in L2 instead of waiting on DRAM when it starts.
+      if (p.next_cta > 0) {
+        const uint32_t nx = gridDim.x, ny = gridDim.y;
+        const uint32_t later = blockIdx.y * nx + blockIdx.x + p.next_cta;
+        if (later < nx * ny) {
+          const int key0_l = static_cast<int>(later % nx) * kKeys;
+          const int bh_l = static_cast<int>(later / nx);
+          const int q0_l = p.mask_kind == kMaskCausal ? key0_l : 0;
+#pragma unroll
+          for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, key0_l, bh_l);
+#pragma unroll
+          for (int b = 0; b < TV::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_v, b * TV::L::kBoxCols, key0_l, bh_l);
+#pragma unroll
+          for (int b = 0; b < TQ::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_q, b * TQ::L::kBoxCols, q0_l, bh_l);
+#pragma unroll
+          for (int b = 0; b < TG::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_g, b * TG::L::kBoxCols, q0_l, bh_l);
+        }
+      }
       mbar_arrive_expect_tx(&bars.kv_full, TK::kBytes + TV::kBytes);
 #pragma unroll
       for (int b = 0; b < TK::L::kBoxes; ++b)

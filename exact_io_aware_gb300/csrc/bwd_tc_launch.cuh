@@ -24,14 +24,15 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   const uint64_t heads = static_cast<uint64_t>(a.B) * a.H;
   constexpr uint32_t bc = RowLayout<D>::kBoxCols;
   constexpr uint32_t bcv = RowLayout<DV>::kBoxCols;
-  CUtensorMap tq, tk, tv, tg, tdk, tdv, tdq;
+  CUtensorMap tq, tk, tv, tg, tdk, tdv, tdq, to;
   if (!encode_tile_map(&tq, a.q, kBf16, heads, a.n, D, 128, bc) ||
       !encode_tile_map(&tg, a.d_o, kBf16, heads, a.n, DV, 128, bcv) ||
       !encode_tile_map(&tk, a.k, kBf16, heads, a.n, D, 128, bc) ||
       !encode_tile_map(&tv, a.v, kBf16, heads, a.n, DV, 128, bcv) ||
       !encode_tile_map(&tdk, a.dk, kBf16, heads, a.n, D, 128, bc) ||
       !encode_tile_map(&tdv, a.dv, kBf16, heads, a.n, DV, 128, bcv) ||
-      !encode_tile_map(&tdq, a.dq, kBf16, heads, a.n, D, 128, bc)) {
+      !encode_tile_map(&tdq, a.dq, kBf16, heads, a.n, D, 128, bc) ||
+      !encode_tile_map(&to, a.o, kBf16, heads, a.n, DV, 128, bcv)) {
     err = "cuTensorMapEncodeTiled rejected a backward tensor map";
     return -5;
   }
@@ -41,6 +42,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
               L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.q,
               a.status};
   p.drop = a.drop;
+  p.next_cta = a.sms;
   // the dK/dV kernel issues S_{i+1} before dK_i releases stage i, and the dQ kernel S_{i+1}
   // before dQ_i releases K_i: those rings need two stages
   p.ring_q = Ring::make(ring_depth(a.ring_stages, 2, Cfg::NS));
@@ -52,7 +54,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   cudaError_t e = cudaFuncSetAttribute(qkern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(qsmem));
   if (e == cudaSuccess) {
-    qkern<<<grid, dq::kThreads, qsmem, s>>>(tk, tv, tdq, p);
+    qkern<<<grid, dq::kThreads, qsmem, s>>>(tk, tv, tdq, tq, tg, to, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) {

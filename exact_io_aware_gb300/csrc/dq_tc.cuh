@@ -130,7 +130,9 @@ __device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&w)[N]) 
 template <bool kBf16, int D, int DV, bool kDrop, bool kCap = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                 const __grid_constant__ CUtensorMap tm_dq, bwd::BwdParams p) {
+                 const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_q,
+                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_o,
+                 bwd::BwdParams p) {
   using C = Config<D, DV>;
   using TQ = typename C::TQ;
   using TK = typename C::TK;
@@ -246,6 +248,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto key0_at = [&](int i) { return static_cast<int>(step_at(i) & 0xFFFFu) * BN; };
   if (warp == kKProducerWarp) {
     // ---------------------------------------------------------------- TMA producer: K
+    // The CTA launched p.next_cta after this one (one per SM, in launch order) finds the rows
+    // its softmax warps load first (Q, dO, O) and its first key block in L2 when it starts.
+    if (lane == 0 && p.next_cta > 0) {
+      const uint32_t nx = gridDim.x, ny = gridDim.y;
+      const uint32_t later = blockIdx.y * nx + blockIdx.x + p.next_cta;
+      if (later < nx * ny) {
+        const int row0_l = (static_cast<int>(nx) - 1 - static_cast<int>(later % nx)) * kRows;
+        const int bh_l = static_cast<int>(later / nx);
+#pragma unroll
+        for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_q, b * TK::L::kBoxCols, row0_l, bh_l);
+#pragma unroll
+        for (int b = 0; b < TV::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_g, b * TV::L::kBoxCols, row0_l, bh_l);
+#pragma unroll
+        for (int b = 0; b < TV::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_o, b * TV::L::kBoxCols, row0_l, bh_l);
+#pragma unroll
+        for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, 0, bh_l);
+#pragma unroll
+        for (int b = 0; b < TV::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_v, b * TV::L::kBoxCols, 0, bh_l);
+      }
+    }
     if (lane == 0 && nsteps > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);

@@ -319,6 +319,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + t * C::kQSlot + b * TQ::kBoxBytes, &tm_q, &bars.q_full[t],
                       b * TQ::L::kBoxCols, pair_row0 + t * kRowsPerTile, bh);
       }
+      // The CTA launched p.next_cta after this one (CTAs start in launch order, one per SM)
+      // finds its query tiles in L2: a fresh CTA's first loads come from DRAM at its share of
+      // the HBM bandwidth, which would otherwise hold it ~3 us before its first product.
+      if (p.next_cta > 0) {
+        const uint32_t nx = gridDim.x, ny = gridDim.y;
+        const uint32_t later = (blockIdx.z * ny + blockIdx.y) * nx + blockIdx.x + p.next_cta;
+        if (later < nx * ny * gridDim.z) {
+          const int row_l = (static_cast<int>(nx) - 1 - static_cast<int>(later % nx)) * p.rows_cta;
+          const int bh_l = static_cast<int>((later / nx) % ny);
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int r0 = row_l + t * kRowsPerTile;
+            if (r0 >= n || r0 >= row_l + p.rows_cta) continue;
+#pragma unroll
+            for (int b = 0; b < TQ::L::kBoxes; ++b)
+              tma_prefetch_l2_3d(&tm_q, b * TQ::L::kBoxCols, r0, bh_l);
+          }
+        }
+      }
       // Ring loads in the order K_0, K_1, V_0, K_2, V_1, ...: K, which the next step waits
       // on first, stays one block ahead of V.
       auto key0_at = [&](int i) { return static_cast<int>(step_at(i) & 0xFFFFu) * BN; };

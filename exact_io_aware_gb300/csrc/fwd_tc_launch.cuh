@@ -45,6 +45,7 @@ int run(const AttnArgs& a, cudaStream_t s, std::string& err) {
   p.ring_k = Ring::make(ring_depth(a.ring_stages, 1, Cfg::NSK));
   p.ring_v = Ring::make(ring_depth(a.ring_stages, 1, Cfg::NSV));
   p.rows_cta = a.fwd_rows_cta == kRowsPerTile ? kRowsPerTile : 2 * kRowsPerTile;
+  p.next_cta = a.sms;
   dim3 grid((a.n + p.rows_cta - 1) / p.rows_cta, static_cast<unsigned>(heads),
             static_cast<unsigned>(nsplit));
   kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);

@@ -85,6 +85,8 @@ struct FwdParams {
   int prefetch;      // key blocks requested into L2 ahead of the ring loads (0: none)
   Ring ring_k, ring_v;  // depths of the K and V rings
   int rows_cta;      // query rows per CTA: 256 (two tiles), or 128 when a grid is small
+  int next_cta;      // CTAs resident at once (the SM count): the CTA launched that many after
+                     // this one has its first tiles requested into L2 (0: none)
 };
 
 // Everything a launcher needs; pointers are device pointers.
@@ -118,6 +120,7 @@ struct AttnArgs {
   DropoutArgs drop;
   int ring_stages;  // cap on the depth of every shared-memory ring (0: as deep as memory allows)
   int fwd_rows_cta;  // forward: query rows per CTA (256, or 128 for grids under half the SMs)
+  int sms;           // multiprocessors of the device
 };
 
 // Each launcher returns 0 or a negative ATTN_ERR_* code and fills `err` on failure.
