@@ -77,12 +77,11 @@ struct BwdParams {
 
 __host__ __device__ constexpr int pad32(int x) { return x < 32 ? 32 : x; }
 
-// Column (within an S or dP buffer) of the 16-bit pair holding query column c.  Each half of
-// the block's queries packs its pairs at the start of its own fp32 column range, so the two
-// softmax warps sharing a lane quadrant never overwrite columns the other still reads.
-__host__ __device__ constexpr int packed_col(int c) {
-  return (c / (BQ / 2)) * (BQ / 2) + (c % (BQ / 2)) / 2;
-}
+// Column (within an S or dP buffer) of the 16-bit pair holding column c (a query of Sᵀ, a key
+// of dP).  Each 32-column chunk packs its pairs into the first 16 of its own fp32 columns: a
+// softmax warp owns whole chunks, so the two warps sharing a lane quadrant never overwrite
+// columns the other still reads.  The 16 columns of one k-step stay 8 adjacent words.
+__host__ __device__ constexpr int packed_col(int c) { return (c / 32) * 32 + (c % 32) / 2; }
 
 // D: width of Q, K, dK rows; DV: width of V, dO, dV rows (the value width).
 template <int D, int DV>
@@ -125,8 +124,8 @@ struct Config {
 
 struct Barriers {
   uint64_t kv_full;
-  uint64_t qdo_full[4], qdo_empty[4], ld_full[4];
-  uint64_t s_full, p_full, dp_full, ds_full;
+  uint64_t q_full[4], g_full[4], q_empty[4], g_empty[4], ld_full[4];
+  uint64_t s_full, p_full[2], dp_full, ds_full;  // p_full[t]: queries 64 t .. 64 t + 63
   uint64_t kv_done;
   uint32_t tmem_base;
   uint32_t nsteps;
@@ -205,12 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&bars.kv_full, 1);
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars.qdo_full[s], 1);
-      mbar_init(&bars.qdo_empty[s], 1);
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.g_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.g_empty[s], 1);
       mbar_init(&bars.ld_full[s], 32);
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, kSoftmaxWarps);
+    mbar_init(&bars.p_full[0], kSoftmaxWarps);
+    mbar_init(&bars.p_full[1], kSoftmaxWarps);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.ds_full, kSoftmaxWarps);
     mbar_init(&bars.kv_done, 1);
@@ -317,17 +319,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nsteps; ++i) {
       const int s = ring_q.stage(i);
       const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
-      if (!mbar_wait_spin(&bars.qdo_empty[s], ring_q.parity(i) ^ 1, p.status, 21)) break;
+      // dO's stage is free once dV of the step NS before has read it, about a product's time
+      // before Q's stage (freed by dK): its load goes first, and Q's (which S waits on) then
+      // has the SM's load bandwidth to itself.
+      if (!mbar_wait(&bars.g_empty[s], ring_q.parity(i) ^ 1, p.status, 33)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.qdo_full[s], TQ::kBytes + TG::kBytes);
-#pragma unroll
-        for (int b = 0; b < TQ::L::kBoxes; ++b)
-          tma_load_3d(sQ + s * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.qdo_full[s],
-                      b * TQ::L::kBoxCols, q0, bh);
+        mbar_arrive_expect_tx(&bars.g_full[s], TG::kBytes);
 #pragma unroll
         for (int b = 0; b < TG::L::kBoxes; ++b)
-          tma_load_3d(sG + s * TG::kBytes + b * TG::kBoxBytes, &tm_g, &bars.qdo_full[s],
+          tma_load_3d(sG + s * TG::kBytes + b * TG::kBoxBytes, &tm_g, &bars.g_full[s],
                       b * TG::L::kBoxCols, q0, bh);
+      }
+      if (!mbar_wait(&bars.q_empty[s], ring_q.parity(i) ^ 1, p.status, 21)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.q_full[s], TQ::kBytes);
+#pragma unroll
+        for (int b = 0; b < TQ::L::kBoxes; ++b)
+          tma_load_3d(sQ + s * TQ::kBytes + b * TQ::kBoxBytes, &tm_q, &bars.q_full[s],
+                      b * TQ::L::kBoxCols, q0, bh);
       }
       if (lane == 0) {
         // rows q0 .. q0+BQ-1 of the row table (always inside the padded table)
@@ -366,9 +375,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dk = TK::desc_k(smem_u32(sK), 0), dv = TV::desc_k(smem_u32(sV), 0);
     const uint64_t dq0 = TQ::desc_k(smem_u32(sQ), 0), dg0 = TG::desc_k(smem_u32(sG), 0);
     const uint64_t dqmn0 = TQ::desc_mn(smem_u32(sQ), 0), dgmn0 = TG::desc_mn(smem_u32(sG), 0);
-    bool ok = mbar_wait_spin_warp(&bars.kv_full, 0, p.status, 22);
-    auto wait_qdo = [&](int i) -> bool {
-      return mbar_wait_spin_warp(&bars.qdo_full[ring_q.stage(i)], ring_q.parity(i), p.status, 23);
+    bool ok = mbar_wait_warp(&bars.kv_full, 0, p.status, 22);
+    auto wait_q = [&](int i) -> bool {
+      return mbar_wait_warp(&bars.q_full[ring_q.stage(i)], ring_q.parity(i), p.status, 23);
+    };
+    auto wait_g = [&](int i) -> bool {
+      return mbar_wait_warp(&bars.g_full[ring_q.stage(i)], ring_q.parity(i), p.status, 34);
     };
     auto issue_s = [&](int i) {
       const uint64_t dq = dq0 + static_cast<uint64_t>(ring_q.stage(i)) * kStage;
@@ -391,34 +403,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     if (ok && nsteps > 0) {
-      ok = wait_qdo(0);
+      ok = wait_q(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp(0);
+        ok = wait_g(0);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+        }
       }
     }
     for (int i = 0; i < nsteps && ok; ++i) {
       const int s = ring_q.stage(i);
-      ok = mbar_wait_spin_warp(&bars.p_full, i & 1, p.status, 24);
-      if (!ok) break;
-      tc_fence_after();
+      // dV in two halves of four k-steps, each as soon as its 64 queries of P are stored
       const uint64_t dgmn = dgmn0 + static_cast<uint64_t>(s) * kStageG;
-      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), dgmn + TG::mn_step(kk),
-                 id_dv, (i > 0 || kk > 0) ? 1u : 0u);
+      for (int t = 0; t < 2 && ok; ++t) {
+        ok = mbar_wait_warp(&bars.p_full[t], i & 1, p.status, 24);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 4 * t; kk < 4 * t + 4; ++kk)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + packed_col(16 * kk), dgmn + TG::mn_step(kk),
+                   id_dv, (i > 0 || kk > 0) ? 1u : 0u);
+          if (t == 1) mma_commit(&bars.g_empty[s]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      if (!ok) break;
       const bool more = i + 1 < nsteps;
       if (more) {
-        ok = wait_qdo(i + 1);
+        ok = wait_q(i + 1);
         if (!ok) break;
         tc_fence_after();
         issue_s(i + 1);
       }
-      ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 25);
+      ok = mbar_wait_warp(&bars.ds_full, i & 1, p.status, 25);
       if (!ok) break;
       tc_fence_after();
       const uint64_t dqmn = dqmn0 + static_cast<uint64_t>(s) * kStage;
@@ -427,10 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BQ / 16; ++kk)
           mma_ts(tmem + C::kColDK, tmem + C::kColDP + packed_col(16 * kk), dqmn + TQ::mn_step(kk),
                  id_dk, (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars.qdo_empty[s]);
+        mma_commit(&bars.q_empty[s]);
       }
       __syncwarp();
-      if (more) issue_dp(i + 1);
+      if (more) {
+        ok = wait_g(i + 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(i + 1);
+      }
     }
     if (elect_one()) mma_commit(&bars.kv_done);
     __syncwarp();
@@ -440,9 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;  // key row within the tile = TMEM lane
     const int j = key0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    constexpr int kHalf = BQ / 2;  // query columns of this warp: [c_lo, c_lo + kHalf)
+    // The two warps of a lane quadrant split the query columns in 32-column chunks: chunk t of
+    // this warp is [64 t + 32 half, + 32).  Chunk 0 of both warps is queries 0 .. 63, the first
+    // four k-steps of dV, which the tensor core starts while the chunks 1 are computed.
+    constexpr int kChunks = BQ / 64;
+    static_assert(BQ == 128, "two 32-column chunks per warp");
     const int half = (warp - kFirstSoftmaxWarp) / 4;
-    const int c_lo = half * kHalf;
+    auto col0 = [&](int t) { return 64 * t + 32 * half; };
     const float sl2 = p.c * 1.4426950408889634f;
     const uint32_t tS = tmem + C::kColS + lane_off;
     const uint32_t tP = tmem + C::kColDP + lane_off;
@@ -455,40 +486,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* Dd = sD + stg * BQ;
       ok = mbar_wait_spin(&bars.ld_full[stg], ring_q.parity(i), p.status, 32);
       if (!ok) break;
-      // Dropout: keep bits of this key with the warp's query columns (bit k of word h <->
-      // query q0 + c_lo + 32 h + k), drawn while the scores are still being computed.  One
+      // Dropout: keep bits of this key with the warp's query columns (bit k of word t <->
+      // query q0 + col0(t) + k), drawn while the scores are still being computed.  One
       // generator call decides a 4 x 4 patch of (query, key) pairs; the four lanes of a key
       // group (keys 4 g .. 4 g + 3, lanes 4 a .. 4 a + 3) share its calls: lane s draws the
-      // patches of queries q0 + c_lo + 16 s .. + 15 and the group exchanges the columns.
-      uint32_t kbits[kDrop ? kHalf / 32 : 1];
+      // patches of queries q0 + col0(s / 2) + 16 (s % 2) .. + 15 and the group exchanges them.
+      uint32_t kbits[kDrop ? kChunks : 1];
       if constexpr (kDrop) {
         uint32_t part[4];
-        keep_cols<kHalf / 16>(p.drop, static_cast<uint32_t>(q0 + c_lo) >> 2,
-                              static_cast<uint32_t>(j) >> 2, bh, part);
-#pragma unroll
-        for (int h = 0; h < kHalf / 32; ++h) kbits[h] = 0u;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) kbits[(s * kHalf / 4) / 32] |= part[s] << ((s * kHalf / 4) % 32);
+        keep_cols<4>(p.drop, static_cast<uint32_t>(q0 + col0(0)) >> 2, static_cast<uint32_t>(q0 + col0(1)) >> 2,
+                     static_cast<uint32_t>(j) >> 2, bh, part);
+        kbits[0] = part[0] | part[1] << 16;
+        kbits[1] = part[2] | part[3] << 16;
       }
       ok = mbar_wait_spin(&bars.s_full, i & 1, p.status, 27);
       if (!ok) break;
       tc_fence_after();
-      uint32_t pkeep[kHalf / 2];  // this warp's P pairs, kept for the dS pass
-      // both 32-column chunks are loaded before one wait: the load latency is paid once
-      uint32_t rr[kHalf / 32][32];
+      uint32_t pkeep[kChunks * 16];  // this warp's P pairs, kept for the dS pass
+      // both chunks are loaded before one wait: the load latency is paid once
+      uint32_t rr[kChunks][32];
 #pragma unroll
-      for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tS + c_lo + 32 * h, rr[h]);
+      for (int t = 0; t < kChunks; ++t) tmem_ld32(tS + col0(t), rr[t]);
       tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < kHalf; cc += 32) {
-        const int c0 = c_lo + cc;
+      for (int t = 0; t < kChunks; ++t) {
+        const int c0 = col0(t);
         float pv[32];
         // The block's LSE values are the same for every lane: 16-byte loads take a quarter of
         // the shared-memory cycles of scalar ones, cycles the products' operand reads need.
         float lv[32];
         load32(L + c0, lv);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[cc / 32][k]) * sl2 - lv[k]);
+        for (int k = 0; k < 32; ++k) pv[k] = ex2(__uint_as_float(rr[t][k]) * sl2 - lv[k]);
         // Masking is a separate pass over the chunk so the common (full-block) path above
         // stays one compact run of instructions.
         if (partial) {
@@ -510,42 +539,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          pkeep[cc / 2 + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
+          pkeep[16 * t + k] = pack2<kBf16>(pv[2 * k], pv[2 * k + 1]);
           if constexpr (kDrop) {
-            const uint32_t kb = kbits[cc / 32] >> (2 * k);
+            const uint32_t kb = kbits[t] >> (2 * k);
             pk[k] = pack2<kBf16>(kb & 1u ? pv[2 * k] : 0.0f, kb & 2u ? pv[2 * k + 1] : 0.0f);
           } else {
-            pk[k] = pkeep[cc / 2 + k];
+            pk[k] = pkeep[16 * t + k];
           }
         }
         tmem_st16(tS + packed_col(c0), pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.p_full[t]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full);
 
       ok = mbar_wait_spin(&bars.dp_full, i & 1, p.status, 28);
       if (!ok) break;
       tc_fence_after();
-      uint32_t dp[kHalf / 32][32];
+      uint32_t dp[kChunks][32];
 #pragma unroll
-      for (int h = 0; h < kHalf / 32; ++h) tmem_ld32(tP + c_lo + 32 * h, dp[h]);
+      for (int t = 0; t < kChunks; ++t) tmem_ld32(tP + col0(t), dp[t]);
       tmem_wait_ld();
 #pragma unroll
-      for (int cc = 0; cc < kHalf; cc += 32) {
-        const int c0 = c_lo + cc;
+      for (int t = 0; t < kChunks; ++t) {
+        const int c0 = col0(t);
         uint32_t pk[16];
         float dv[32];
         load32(Dd + c0, dv);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           float p0, p1;
-          unpack2<kBf16>(pkeep[cc / 2 + k], p0, p1);
-          float d0 = __uint_as_float(dp[cc / 32][2 * k]);
-          float d1 = __uint_as_float(dp[cc / 32][2 * k + 1]);
+          unpack2<kBf16>(pkeep[16 * t + k], p0, p1);
+          float d0 = __uint_as_float(dp[t][2 * k]);
+          float d1 = __uint_as_float(dp[t][2 * k + 1]);
           if constexpr (kDrop) {
-            const uint32_t kb = kbits[cc / 32] >> (2 * k);
+            const uint32_t kb = kbits[t] >> (2 * k);
             d0 = kb & 1u ? d0 * p.drop.scale : 0.0f;
             d1 = kb & 2u ? d1 * p.drop.scale : 0.0f;
           }

@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v);
       for (int i = 0; i < nsteps; ++i) {
         const int s = ring_k.stage(i);
-        if (!mbar_wait_spin(&bars.k_empty[s], ring_k.parity(i) ^ 1, p.status, 42)) break;
+        if (!mbar_wait(&bars.k_empty[s], ring_k.parity(i) ^ 1, p.status, 42)) break;
         mbar_arrive_expect_tx(&bars.k_full[s], TK::kBytes);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b)
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       for (int i = 0; i < nsteps; ++i) {
         const int s = ring_v.stage(i);
-        if (!mbar_wait_spin(&bars.v_empty[s], ring_v.parity(i) ^ 1, p.status, 41)) break;
+        if (!mbar_wait(&bars.v_empty[s], ring_v.parity(i) ^ 1, p.status, 41)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], TV::kBytes);
 #pragma unroll
         for (int b = 0; b < TV::L::kBoxes; ++b)
@@ -312,10 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint64_t kStageV = TV::kBytes >> 4;
     const uint64_t dk0 = TK::desc_k(smem_u32(sK), 0), dv0 = TV::desc_k(smem_u32(sV), 0);
     const uint64_t dkmn0 = TK::desc_mn(smem_u32(sK), 0);
-    bool ok = nsteps == 0 || mbar_wait_spin_warp(&bars.qg_full, 0, p.status, 43);
+    bool ok = nsteps == 0 || mbar_wait_warp(&bars.qg_full, 0, p.status, 43);
     auto issue_s = [&](int i) -> bool {
       const int ks = ring_k.stage(i);
-      if (!mbar_wait_spin_warp(&bars.k_full[ks], ring_k.parity(i), p.status, 44)) return false;
+      if (!mbar_wait_warp(&bars.k_full[ks], ring_k.parity(i), p.status, 44)) return false;
       tc_fence_after();
       const uint64_t dk = dk0 + static_cast<uint64_t>(ks) * kStage;
       if (elect_one()) {
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_dp = [&](int i) -> bool {
       const int vs = ring_v.stage(i);
-      if (!mbar_wait_spin_warp(&bars.v_full[vs], ring_v.parity(i), p.status, 45)) return false;
+      if (!mbar_wait_warp(&bars.v_full[vs], ring_v.parity(i), p.status, 45)) return false;
       tc_fence_after();
       const uint64_t dv = dv0 + static_cast<uint64_t>(vs) * kStageV;
       if (elect_one()) {
@@ -347,13 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nsteps && ok; ++i) {
       if (i + 1 < nsteps) {
         // S_{i+1} overwrites S_i: wait until every softmax warp has loaded it
-        ok = mbar_wait_spin_warp(&bars.s_free, i & 1, p.status, 50);
+        ok = mbar_wait_warp(&bars.s_free, i & 1, p.status, 50);
         if (!ok) break;
         tc_fence_after();
         ok = issue_s(i + 1);
         if (!ok) break;
       }
-      ok = mbar_wait_spin_warp(&bars.ds_full, i & 1, p.status, 46);
+      ok = mbar_wait_warp(&bars.ds_full, i & 1, p.status, 46);
       if (!ok) break;
       tc_fence_after();
       const int ks = ring_k.stage(i);
@@ -510,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the patches of keys key0 + c_lo + 16 s .. + 15
         uint32_t part[4];
         keep_rows<kHalf / 16>(p.drop, static_cast<uint32_t>(row) >> 2,
-                              static_cast<uint32_t>(key0 + c_lo) >> 2, bh, part);
+                              static_cast<uint32_t>(key0 + c_lo) >> 2,
+                              (static_cast<uint32_t>(key0 + c_lo) >> 2) + kHalf / 8, bh, part);
 #pragma unroll
         for (int h = 0; h < kHalf / 32; ++h) kbits[h] = 0u;
 #pragma unroll

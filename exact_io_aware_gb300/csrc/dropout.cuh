@@ -77,20 +77,23 @@ __device__ __forceinline__ void exchange4(const uint32_t (&w)[4], uint32_t (&par
   for (uint32_t s = 0; s < 4; ++s) part[s] = pick4(recv, s ^ sub);
 }
 
-// Keep bits of one row for a run of 4 K consecutive keys, drawn by the four lanes of an aligned
-// group (lanes 4a .. 4a + 3, holding rows 4 r .. 4 r + 3 in lane order): lane s of the group
-// draws the K patches of keys 4 (g0 + s K) .. + 4 K, and three exchanges give every lane the
-// K-nibble words of its own row.  part[s] receives keys 4 (g0 + s K) .. of this lane's row, bit
-// 4 u + y <-> key 4 (g0 + s K + u) + y.  Warp-collective: every lane must call it.
+// Keep bits of one row for two runs of 2 K keys each, drawn by the four lanes of an aligned
+// group (lanes 4a .. 4a + 3, holding rows 4 r .. 4 r + 3 in lane order): lanes 0 and 1 of the
+// group draw the K patches of keys 4 (g0 + s K) .. + 4 K, lanes 2 and 3 those of keys
+// 4 (g1 + (s - 2) K) .., and three exchanges give every lane the K-nibble words of its own row.
+// part[s] receives lane s's keys of this lane's row, bit 4 u + y <-> the u-th patch's key y.
+// With g1 = g0 + 2 K the four lanes cover one run of 16 K keys.  Warp-collective: every lane
+// must call it.
 template <int K>
 __device__ __forceinline__ void keep_rows(const DropoutArgs& dr, uint32_t r, uint32_t g0,
-                                         uint32_t bh, uint32_t (&part)[4]) {
+                                         uint32_t g1, uint32_t bh, uint32_t (&part)[4]) {
   static_assert(4 * K <= 32, "at most 32 keys per lane");
   const uint32_t sub = threadIdx.x & 3u;
+  const uint32_t gb = sub < 2u ? g0 + sub * K : g1 + (sub - 2u) * K;
   uint32_t w[4] = {0u, 0u, 0u, 0u};  // w[x]: row 4 r + x over this lane's keys
 #pragma unroll 1
   for (int u = 0; u < K; ++u) {
-    const uint32_t m = keep_patch(dr, r, g0 + sub * K + u, bh);
+    const uint32_t m = keep_patch(dr, r, gb + u, bh);
 #pragma unroll
     for (int x = 0; x < 4; ++x) w[x] |= ((m >> (4 * x)) & 0xFu) << (4 * u);
   }
@@ -98,17 +101,19 @@ __device__ __forceinline__ void keep_rows(const DropoutArgs& dr, uint32_t r, uin
 }
 
 // The same for a key-major layout (one key per lane): the four lanes of an aligned group hold
-// keys 4 g .. 4 g + 3, lane s draws the K patches of rows 4 (r0 + s K) .. + 4 K, and part[s]
-// receives this lane's key over those rows, bit 4 u + x <-> row 4 (r0 + s K + u) + x.
+// keys 4 g .. 4 g + 3; lanes 0 and 1 draw the K patches of rows 4 (r0 + s K) .. + 4 K, lanes 2
+// and 3 those of rows 4 (r1 + (s - 2) K) .., and part[s] receives this lane's key over lane s's
+// rows, bit 4 u + x <-> the u-th patch's row x.
 template <int K>
-__device__ __forceinline__ void keep_cols(const DropoutArgs& dr, uint32_t r0, uint32_t g,
-                                         uint32_t bh, uint32_t (&part)[4]) {
+__device__ __forceinline__ void keep_cols(const DropoutArgs& dr, uint32_t r0, uint32_t r1,
+                                         uint32_t g, uint32_t bh, uint32_t (&part)[4]) {
   static_assert(4 * K <= 32, "at most 32 rows per lane");
   const uint32_t sub = threadIdx.x & 3u;
+  const uint32_t rb = sub < 2u ? r0 + sub * K : r1 + (sub - 2u) * K;
   uint32_t w[4] = {0u, 0u, 0u, 0u};  // w[y]: key 4 g + y over this lane's rows
 #pragma unroll 1
   for (int u = 0; u < K; ++u) {
-    const uint32_t m = keep_patch(dr, r0 + sub * K + u, g, bh);
+    const uint32_t m = keep_patch(dr, rb + u, g, bh);
     // column y of the patch: bits y, 4 + y, 8 + y, 12 + y -> one nibble (multiply places them on
     // bits 12 .. 15: the partial products fall on distinct bits)
 #pragma unroll

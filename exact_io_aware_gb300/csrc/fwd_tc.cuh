@@ -486,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rows 4 r .. 4 r + 3 are lanes 4 a .. 4 a + 3 (the warp's rows start at a multiple of
         // 32); lane s of such a group draws the generator calls of keys key0 + s BN / 4 ..
         uint32_t part[4];
-        keep_rows<BN / 16>(p.drop, static_cast<uint32_t>(row) >> 2,
-                           static_cast<uint32_t>(key0) >> 2, bh, part);
+        keep_rows<BN / 16>(p.drop, static_cast<uint32_t>(row) >> 2, static_cast<uint32_t>(key0) >> 2,
+                           (static_cast<uint32_t>(key0) >> 2) + BN / 8, bh, part);
 #pragma unroll
         for (int q = 0; q < BN / 32; ++q) kbits[q] = 0u;
 #pragma unroll
