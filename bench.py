@@ -66,7 +66,7 @@ def kernel_source_digest():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith(("bwd_tc", "dq_tc", "tile", "ptx")):
+        if name.startswith(("bwd_tc", "dq_tc", "tile", "ptx", "dropout")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
