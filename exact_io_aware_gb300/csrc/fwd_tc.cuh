@@ -493,16 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < 4; ++s) kbits[(s * BN / 4) / 32] |= part[s] << ((s * BN / 4) % 32);
       }
-      ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
-      if (!ok) break;
-      s_phase ^= 1;
-      tc_fence_after();
-      // Masking (partial blocks only), done in tensor memory before the scores are read: each
-      // 32-key chunk is loaded, its masked entries set to the raw value whose scaled image is
-      // -inf, and stored back.  A rolled loop keeps this rare path small, so the common path
-      // below stays one compact run of instructions.
+      // Masking (partial blocks only): the block's allowed-key words (bit k of word q <-> key
+      // key0 + 32 q + k), formed while the scores are still being computed and applied to the
+      // scores in registers below.
+      uint32_t mw[BN / 32];
       if (__builtin_expect(cls == kPartial, 0)) {
-#pragma unroll 1
+#pragma unroll
         for (int q = 0; q < BN / 32; ++q) {
           const int kq = key0 + q * 32;
           uint32_t w;
@@ -516,17 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cnt = min(max(lim - kq + 1, 0), 32);
             w = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
           }
-          uint32_t rr[32];
-          tmem_ld32(tS + lane_off + q * 32, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (!((w >> k) & 1u)) rr[k] = __float_as_uint(mv);
-          tmem_st16(tS + lane_off + q * 32, *reinterpret_cast<const uint32_t(*)[16]>(rr));
-          tmem_st16(tS + lane_off + q * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(rr + 16));
+          mw[q] = w;
         }
-        tmem_wait_st();
       }
+      ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
+      if (!ok) break;
+      s_phase ^= 1;
+      tc_fence_after();
       // All TMEM loads first, one wait: the row's BN raw scores land in registers.
       float sv[BN];
       {
@@ -537,6 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < BN; ++k) sv[k] = __uint_as_float(rr[k]);
+      }
+      // masked entries take the raw value whose scaled image is -inf
+      if (__builtin_expect(cls == kPartial, 0)) {
+#pragma unroll
+        for (int k = 0; k < BN; ++k)
+          if (!((mw[k / 32] >> (k % 32)) & 1u)) sv[k] = mv;
       }
       // Row extreme of the raw scores with four independent accumulators (short chains).
       float a0 = mv, a1 = mv, a2 = mv, a3 = mv;
