@@ -382,12 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         lr = __log2f(__ldg(p.sv_blk + sbase + jb)) - l2vmax;
         inv_r = ex2(-lr);
       }
-      ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
-      if (!ok) break;
-      s_phase ^= 1;
-      tc_fence_after();
+      // partial blocks: the allowed-key words (bit k of word q <-> key key0 + 32 q + k), applied
+      // to the scores in registers once they are loaded
+      uint32_t mw[BN / 32];
       if (cls == kPartial) {
-#pragma unroll 1
+#pragma unroll
         for (int q = 0; q < BN / 32; ++q) {
           const int kq = key0 + q * 32;
           uint32_t w;
@@ -400,17 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cnt = min(max(lim - kq + 1, 0), 32);
             w = cnt >= 32 ? 0xFFFFFFFFu : ((1u << cnt) - 1u);
           }
-          uint32_t rr[32];
-          tmem_ld32(tS + lane_off + q * 32, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (!((w >> k) & 1u)) rr[k] = __float_as_uint(mv);
-          tmem_st16(tS + lane_off + q * 32, *reinterpret_cast<const uint32_t(*)[16]>(rr));
-          tmem_st16(tS + lane_off + q * 32 + 16, *reinterpret_cast<const uint32_t(*)[16]>(rr + 16));
+          mw[q] = w;
         }
-        tmem_wait_st();
       }
+      ok = mbar_wait(&bars.s_full[t], s_phase, p.status, 8);
+      if (!ok) break;
+      s_phase ^= 1;
+      tc_fence_after();
       float sv[BN];
       {
         uint32_t rr[BN];
@@ -420,6 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < BN; ++k) sv[k] = __uint_as_float(rr[k]);
+      }
+      // masked entries take the raw value whose scaled image is -inf
+      if (cls == kPartial) {
+#pragma unroll
+        for (int k = 0; k < BN; ++k)
+          if (!((mw[k / 32] >> (k % 32)) & 1u)) sv[k] = mv;
       }
       float a0 = mv, a1 = mv, a2 = mv, a3 = mv;
       if (pos) {
