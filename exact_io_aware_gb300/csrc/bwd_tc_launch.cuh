@@ -44,10 +44,11 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   p.drop = a.drop;
   p.next_cta = a.sms;
   // the dK/dV kernel issues S_{i+1} before dK_i releases stage i, and the dQ kernel S_{i+1}
-  // before dQ_i releases K_i: those rings need two stages
+  // before dQ_i releases K_i: those rings need two stages; the dQ kernel's V ring stages the
+  // tile's dO and O in its last two stages at the start
   p.ring_q = Ring::make(ring_depth(a.ring_stages, 2, Cfg::NS));
   p.ring_k = Ring::make(ring_depth(a.ring_stages, 2, QCfg::NSK));
-  p.ring_v = Ring::make(ring_depth(a.ring_stages, 1, QCfg::NSV));
+  p.ring_v = Ring::make(ring_depth(a.ring_stages, 2, QCfg::NSV));
   const dim3 grid((a.n + 127) / 128, static_cast<unsigned>(heads));
   // the dQ kernel writes the row table the dK/dV kernel reads
   auto qkern = dq::dq_tc_kernel<kBf16, D, DV, kDrop, kCap>;

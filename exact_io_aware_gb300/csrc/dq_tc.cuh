@@ -102,6 +102,8 @@ struct Config {
 
 struct Barriers {
   uint64_t qg_full;  // Q and dO are in tensor memory (one arrival per softmax warp)
+  uint64_t st_full;  // the tile's Q, dO and O have arrived in shared memory (TMA bytes)
+  uint64_t st_free;  // the softmax warps have read them (one arrival per softmax warp)
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full, s_free, dp_full, ds_full;
   uint64_t dq_done;
@@ -141,6 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int NSV = C::NSV;
   const auto ring_k = ring_of<kCap, NSK>(p.ring_k);
   const auto ring_v = ring_of<kCap, NSV>(p.ring_v);
+  // stages of the V ring in use; the last two hold the tile's dO and O at the start
+  const int nv = kCap ? static_cast<int>(p.ring_v.n) : NSV;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = bwd::align1024(smem_raw);
@@ -162,6 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- prologue
   if (tid == 0) {
     mbar_init(&bars.qg_full, kSoftmaxWarps);
+    mbar_init(&bars.st_full, 1);
+    mbar_init(&bars.st_free, kSoftmaxWarps);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
@@ -291,8 +297,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kVProducerWarp) {
     // ---------------------------------------------------------------- TMA producer: V
     if (lane == 0) {
+      // The tile's Q (into the dQ staging slot), dO and O (into the last two V stages) for the
+      // softmax warps, which read their rows from there: one bulk copy each instead of every
+      // lane loading its own row.
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_g);
+      tma_prefetch_desc(&tm_o);
+      mbar_arrive_expect_tx(&bars.st_full, TQ::kBytes + 2 * TV::kBytes);
+#pragma unroll
+      for (int b = 0; b < TQ::L::kBoxes; ++b)
+        tma_load_3d(sQ + b * TQ::kBoxBytes, &tm_q, &bars.st_full, b * TQ::L::kBoxCols, row0, bh);
+#pragma unroll
+      for (int b = 0; b < TV::L::kBoxes; ++b)
+        tma_load_3d(sV + (nv - 1) * TV::kBytes + b * TV::kBoxBytes, &tm_g, &bars.st_full,
+                    b * TV::L::kBoxCols, row0, bh);
+#pragma unroll
+      for (int b = 0; b < TV::L::kBoxes; ++b)
+        tma_load_3d(sV + (nv - 2) * TV::kBytes + b * TV::kBoxBytes, &tm_o, &bars.st_full,
+                    b * TV::L::kBoxCols, row0, bh);
       for (int i = 0; i < nsteps; ++i) {
         const int s = ring_v.stage(i);
+        // the last two stages take their first V block once dO and O have been read
+        if (i < nv && s >= nv - 2 && !mbar_wait(&bars.st_free, 0, p.status, 52)) break;
         if (!mbar_wait(&bars.v_empty[s], ring_v.parity(i) ^ 1, p.status, 41)) break;
         mbar_arrive_expect_tx(&bars.v_full[s], TV::kBytes);
 #pragma unroll
@@ -384,25 +410,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - kFirstSoftmaxWarp) / 4;
     const int c_lo = half * kHalf;
     const float sl2 = p.c * 1.4426950408889634f;
-    // D_i: this warp sums dO * O over its half of the value columns (16-byte loads).  The
-    // same dO words, and this half of the row's Q, go into tensor memory as the A operands of
-    // dP and S: memory order puts element 2c in the low half of word c, which is the operand
-    // layout (two 16-bit elements a column).  Rows past n get zeros.
+    // D_i: this warp sums dO * O over its half of the value columns.  The same dO words, and
+    // this half of the row's Q, go into tensor memory as the A operands of dP and S: memory
+    // order puts element 2c in the low half of word c, which is the operand layout (two 16-bit
+    // elements a column).  The rows come from the tiles staged in shared memory (16-byte reads;
+    // rows past n arrive as zeros).
     float dpar = 0.0f;
+    bool ok = mbar_wait_spin(&bars.st_full, 0, p.status, 51);
     {
-      using E = typename std::conditional<kBf16, __nv_bfloat16, __half>::type;
       constexpr int kGW = DV / 4;  // dO columns of this half
       constexpr int kQW = D / 4;   // Q columns of this half
       uint32_t gcol[kGW], qcol[kQW];
-      const bool in = row < n;
-      const int64_t rr = static_cast<int64_t>(bh) * n + (in ? row : 0);
-      const uint4* o4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.o) + rr * DV + half * (DV / 2));
-      const uint4* g4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.d_o) + rr * DV + half * (DV / 2));
-      const uint4* q4 = reinterpret_cast<const uint4*>(static_cast<const E*>(p.q) + rr * D + half * (D / 2));
+      const uint8_t* sG = sV + (nv - 1) * TV::kBytes;
+      const uint8_t* sO = sV + (nv - 2) * TV::kBytes;
 #pragma unroll
       for (int v = 0; v < DV / 16; ++v) {
-        const uint4 a = in ? __ldg(o4 + v) : make_uint4(0u, 0u, 0u, 0u);
-        const uint4 g = in ? __ldg(g4 + v) : make_uint4(0u, 0u, 0u, 0u);
+        const int c = half * (DV / 2) + 8 * v;
+        const uint4 a = *reinterpret_cast<const uint4*>(sO + TV::offset(r, c));
+        const uint4 g = *reinterpret_cast<const uint4*>(sG + TV::offset(r, c));
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -416,12 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int v = 0; v < D / 16; ++v) {
-        const uint4 q = in ? __ldg(q4 + v) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 q = *reinterpret_cast<const uint4*>(sQ + TQ::offset(r, half * (D / 2) + 8 * v));
         qcol[4 * v] = q.x;
         qcol[4 * v + 1] = q.y;
         qcol[4 * v + 2] = q.z;
         qcol[4 * v + 3] = q.w;
       }
+      // dO and O are read: their V stages may take V blocks
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.st_free);
       st_cols<kQW>(tmem + lane_off + C::kColQ + half * kQW, qcol);
       st_cols<kGW>(tmem + lane_off + C::kColG + half * kGW, gcol);
       tmem_wait_st();
@@ -447,7 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             ? p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words +
                   static_cast<int64_t>(row < n ? row : 0) * p.mask_row_words
             : nullptr;
-    bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
       const uint32_t sw = step_at(i);
       const int key0 = static_cast<int>(sw & 0xFFFFu) * BN;
