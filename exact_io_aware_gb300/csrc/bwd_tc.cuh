@@ -62,11 +62,9 @@ struct BwdParams {
   float* L2;
   float* Dv;
   int n_pad;
-  // inputs the dQ kernel builds the table from (and the rows it loads into tensor memory)
+  // the forward's LSE, which the dQ kernel builds the table from (O, dO and Q it reads through
+  // their tensor maps)
   const float* lse;
-  const void* o;
-  const void* d_o;
-  const void* q;
   uint32_t* status;
   DropoutArgs drop;  // read only by the dropout instantiations
   Ring ring_q;          // depth of the dK/dV kernel's (Q, dO, row table) ring
@@ -220,11 +218,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kMmaWarp) tmem_alloc(&bars.tmem_base, C::kTmemAlloc);
 
-  // Classify each query block against this key tile: skip / full / partial.
-  for (int i = tid; i < nqb; i += kThreads) steps[i] = 0;
-  __syncthreads();
+  // Classify each query block against this key tile: skip / full / partial.  Under no mask
+  // or the causal mask the blocks taken are a contiguous run (from the first block holding a
+  // row at or past key0 under causal) and each step is classified on the fly; a bitmap mask
+  // builds a table of the blocks taken.
+  const bool use_table = p.mask_kind == kMaskBitmap;
+  const bool causal = p.mask_kind == kMaskCausal;
   const bool key_tail = key0 + kKeys > n;
-  if (p.mask_kind == kMaskBitmap) {
+  const int first_blk = causal ? key0 / BQ : 0;
+  if (use_table) {
+    for (int i = tid; i < nqb; i += kThreads) steps[i] = 0;
+    __syncthreads();
     if (tid < 256) {
       const int nwords = (min(key0 + kKeys, n) - key0 + 31) / 32;
       for (int q0 = 0; q0 < n; q0 += 256) {
@@ -250,30 +254,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
-    for (int i = tid; i < nqb; i += kThreads) {
-      const int q0 = i * BQ;
-      const int qlast = min(q0 + BQ, n) - 1;
-      bool any = true, all = true;
-      if (p.mask_kind == kMaskCausal) {
-        any = qlast >= key0;
-        all = q0 >= key0 + kKeys - 1;
+    __syncthreads();
+    if (warp == 0) {
+      // compaction in place, 32 blocks a round: a taken block's entry goes to the count of
+      // taken blocks before it, never past its own index
+      int ns = 0;
+      for (int i0 = 0; i0 < nqb; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t b = i < nqb ? steps[i] : 0u;
+        const bool take = (b & 1u) != 0;
+        const bool tail = key_tail || (i + 1) * BQ > n;
+        const uint32_t cls = ((b & 2u) || tail) ? kPartial : kFull;
+        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, take);
+        __syncwarp();
+        if (take) steps[ns + __popc(ballot & ((1u << lane) - 1u))] = static_cast<uint32_t>(i) | (cls << 16);
+        __syncwarp();
+        ns += __popc(ballot);
       }
-      steps[i] = any ? (1u | (all ? 0u : 2u)) : 0u;
+      if (lane == 0) bars.nsteps = ns;
     }
+  } else if (tid == 0) {
+    bars.nsteps = nqb - first_blk;
   }
-  __syncthreads();
-  if (tid == 0) {
-    int ns = 0;
-    for (int i = 0; i < nqb; ++i) {
-      const uint32_t b = steps[i];
-      if (!(b & 1u)) continue;
-      const bool tail = key_tail || (i + 1) * BQ > n;
-      const uint32_t cls = ((b & 2u) || tail) ? kPartial : kFull;
-      steps[ns++] = static_cast<uint32_t>(i) | (cls << 16);
-    }
-    bars.nsteps = ns;
-  }
+  // Step word: query block | class << 16.
+  auto step_at = [&](int i) -> uint32_t {
+    if (use_table) return steps[i];
+    const int j = first_blk + i;
+    const bool all = !causal || j * BQ >= key0 + kKeys - 1;
+    const bool tail = key_tail || (j + 1) * BQ > n;
+    return static_cast<uint32_t>(j) | ((all && !tail ? kFull : kPartial) << 16);
+  };
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < nsteps; ++i) {
       const int s = ring_q.stage(i);
-      const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
+      const int q0 = static_cast<int>(step_at(i) & 0xFFFFu) * BQ;
       // dO's stage is free once dV of the step NS before has read it, about a product's time
       // before Q's stage (freed by dK): its load goes first, and Q's (which S waits on) then
       // has the SM's load bandwidth to itself.
@@ -344,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(sL + s * BQ, l2_h + q0, BQ * 4, &bars.ld_full[s]);
         bulk_load(sD + s * BQ, d_h + q0, BQ * 4, &bars.ld_full[s]);
       }
-      if (p.mask_kind == kMaskBitmap && ((steps[i] >> 16) & 3u) == kPartial) {
+      if (use_table && ((steps[i] >> 16) & 3u) == kPartial) {
         // words of allowed-key bits for rows q0.. of this block and keys key0..key0+127;
         // rows past n and keys past n read as not allowed
         const uint32_t* bits = p.mask_bits + static_cast<int64_t>(bh) * p.mask_head_stride_words;
@@ -479,8 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tP = tmem + C::kColDP + lane_off;
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
-      const int q0 = static_cast<int>(steps[i] & 0xFFFFu) * BQ;
-      const bool partial = ((steps[i] >> 16) & 3u) == kPartial;
+      const uint32_t sw = step_at(i);
+      const int q0 = static_cast<int>(sw & 0xFFFFu) * BQ;
+      const bool partial = ((sw >> 16) & 3u) == kPartial;
       const int stg = ring_q.stage(i);
       const float* L = sL + stg * BQ;
       const float* Dd = sD + stg * BQ;
@@ -528,7 +539,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 32; ++k)
               if (!((wb[4 * k] >> lane) & 1u)) pv[k] = 0.0f;
           } else {
-            const bool causal = p.mask_kind == kMaskCausal;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
               const int q = q0 + c0 + k;

@@ -39,8 +39,7 @@ int run(const AttnArgs& a, float* table, cudaStream_t s, std::string& err) {
   const int n_pad = bwd_pad_rows(a.n);
   float* L2 = table;
   BwdParams p{a.n,  a.c, a.mask_kind, a.mask_bits, a.mask_row_words, a.mask_head_stride_words,
-              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.o, a.d_o, a.q,
-              a.status};
+              L2,   L2 + static_cast<size_t>(heads) * n_pad, n_pad, a.lse, a.status};
   p.drop = a.drop;
   p.next_cta = a.sms;
   // the dK/dV kernel issues S_{i+1} before dK_i releases stage i, and the dQ kernel S_{i+1}

@@ -255,21 +255,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
+      // compaction in place by one warp, 32 blocks a round: a taken block's entry goes to the
+      // count of taken blocks before it, never past its own index
       const bool tail = (nk % BN) != 0;
       int ns = 0;
-      for (int j = j_lo; j < j_hi; ++j) {
-        const uint32_t b = steps[j];
-        const bool part_tail = tail && j == nblk - 1;
-        uint32_t cls0 = (b & 1u) ? (((b & 4u) || part_tail) ? kPartial : kFull) : kSkip;
-        uint32_t cls1 = (b & 2u) ? (((b & 8u) || part_tail) ? kPartial : kFull) : kSkip;
-        if (cls0 | cls1) steps[ns++] = static_cast<uint32_t>(j) | (cls0 << 16) | (cls1 << 18);
-      }
       uint32_t act = 0;
-      for (int i = 0; i < ns; ++i)
-        act |= ((steps[i] >> 16) & 3u ? 1u : 0u) | ((steps[i] >> 18) & 3u ? 2u : 0u);
-      bars.nsteps = ns;
-      bars.act = act;
+      for (int j0 = j_lo; j0 < j_hi; j0 += 32) {
+        const int j = j0 + lane;
+        const uint32_t b = j < j_hi ? steps[j] : 0u;
+        const bool part_tail = tail && j == nblk - 1;
+        const uint32_t cls0 = (b & 1u) ? (((b & 4u) || part_tail) ? kPartial : kFull) : kSkip;
+        const uint32_t cls1 = (b & 2u) ? (((b & 8u) || part_tail) ? kPartial : kFull) : kSkip;
+        const bool take = (cls0 | cls1) != 0u;
+        const uint32_t ballot = __ballot_sync(0xFFFFFFFFu, take);
+        __syncwarp();
+        if (take)
+          steps[ns + __popc(ballot & ((1u << lane) - 1u))] =
+              static_cast<uint32_t>(j) | (cls0 << 16) | (cls1 << 18);
+        __syncwarp();
+        ns += __popc(ballot);
+        act |= (cls0 ? 1u : 0u) | (cls1 ? 2u : 0u);
+      }
+      act = __reduce_or_sync(0xFFFFFFFFu, act);
+      if (lane == 0) {
+        bars.nsteps = ns;
+        bars.act = act;
+      }
     }
   } else if (tid == 0) {
     bars.nsteps = j_hi - j_lo;

@@ -9,6 +9,7 @@ stale or aliased table would show as a changed bit), that it allocates no device
 that it refuses problems larger than its array.  It is collected last on purpose.
 """
 import ctypes
+import gc
 
 import pytest
 import torch
@@ -59,14 +60,20 @@ def test_noalloc_matches_attn_bwd_on_two_calls(dtype):
         ref = ea.attn_bwd(q, k, v, o, lse, g, wl.c, mask="causal")
         code = ea.DTYPE_CODE[q.dtype]
         dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
-        torch.cuda.synchronize()
-        torch_bytes = torch.cuda.memory_allocated()
-        free_before = torch.cuda.mem_get_info()[0]
-        rc = noalloc(code, wl.B, wl.H, wl.n, wl.d, wl.c, _p(q), _p(k), _p(v), _p(o), _p(lse),
-                     _p(g), 1, ctypes.c_void_p(0), 0, 0, 0, _p(dq), _p(dk), _p(dv), stream)
-        assert rc == 0, ea.attn_last_error()
-        assert ea.attn_device_status() == ea.ATTN_OK
-        assert torch.cuda.memory_allocated() == torch_bytes
+        # garbage from earlier tests must not be collected (and freed) inside the measured window
+        gc.collect()
+        gc.disable()
+        try:
+            torch.cuda.synchronize()
+            torch_bytes = torch.cuda.memory_allocated()
+            free_before = torch.cuda.mem_get_info()[0]
+            rc = noalloc(code, wl.B, wl.H, wl.n, wl.d, wl.c, _p(q), _p(k), _p(v), _p(o), _p(lse),
+                         _p(g), 1, ctypes.c_void_p(0), 0, 0, 0, _p(dq), _p(dk), _p(dv), stream)
+            assert rc == 0, ea.attn_last_error()
+            assert ea.attn_device_status() == ea.ATTN_OK
+            assert torch.cuda.memory_allocated() == torch_bytes
+        finally:
+            gc.enable()
         if call == 1:  # the first call may load the library's module data on this device
             assert _free_device_bytes_unchanged(free_before)
         for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
