@@ -163,6 +163,37 @@ __device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
   }
 }
 
+// Rounds kW accumulator columns of this thread's TMEM lane (from taddr) times `scale` to 16-bit
+// pairs and writes them to row r of the staged tile T from column c_first: up to 64 columns
+// are loaded before one wait.  Zeros when `have` is false (no product was accumulated).
+template <bool kBf16, class T, int kW>
+__device__ __forceinline__ void stage_acc(uint32_t taddr, float scale, uint8_t* stage, int r,
+                                          int c_first, bool have) {
+  static_assert(kW % 16 == 0, "16-column loads");
+  constexpr int kB = kW < 64 ? kW : 64;
+#pragma unroll
+  for (int c0 = 0; c0 < kW; c0 += kB) {
+    uint32_t v[kB];
+    if (have) {
+#pragma unroll
+      for (int c = 0; c < kB; c += 16)
+        tmem_ld16(taddr + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int k = 0; k < kB; ++k) v[k] = 0u;
+    }
+#pragma unroll
+    for (int c = 0; c < kB; c += 8) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        pk[k] = pack2<kBf16>(scale * __uint_as_float(v[c + 2 * k]), scale * __uint_as_float(v[c + 2 * k + 1]));
+      *reinterpret_cast<uint4*>(stage + T::offset(r, c_first + c0 + c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+}
+
 // kCap: ring depth from the launch (p.ring_q) instead of the compile-time count.
 template <bool kBf16, int D, int DV, bool kDrop, bool kCap = false>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -599,62 +630,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ds_full);
     }
-    // ---------------------------------------------------------------- epilogue (warps 1-4)
-    // dK = c * (dSᵀ Q), dV = Pᵀ dO, rounded and stored through the (now idle) K/V tiles.
-    if (half == 0) {
-      const float dvs = kDrop ? p.drop.scale : 1.0f;  // dV = (P with dropped pairs zeroed)ᵀ dO / (1-p)
-      if (ok) ok = mbar_wait_spin(&bars.kv_done, 0, p.status, 31);
-      tc_fence_after();
-      if (ok) {
-        // dV (DV columns) into V's tile, then dK (D columns) into K's tile
+    // ---------------------------------------------------------------- epilogue
+    // dV = Pᵀ dO (the warps of half 0) and dK = c * (dSᵀ Q) (half 1), rounded and staged in
+    // the (now idle) V and K tiles, then stored by TMA.
+    if (ok) ok = mbar_wait_spin(&bars.kv_done, 0, p.status, 31);
+    tc_fence_after();
+    if (ok) {
+      if (half == 0)  // dV = (P with dropped pairs zeroed)ᵀ dO / (1-p)
+        stage_acc<kBf16, TV, DV>(tmem + C::kColDV + lane_off, kDrop ? p.drop.scale : 1.0f, sV, r, 0,
+                                 nsteps > 0);
+      else
+        stage_acc<kBf16, TK, D>(tmem + C::kColDK + lane_off, p.c, sK, r, 0, nsteps > 0);
+    }
+    fence_proxy_async_smem();
+    named_barrier(2, kSoftmaxWarps * 32);
+    if (ok && half == 0 && r == 0) {
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 16) {
-          uint32_t rv[16];
-          if (nsteps > 0) {
-            tmem_ld16(tmem + C::kColDV + lane_off + c0, rv);
-            tmem_wait_ld();
-          } else {
+      for (int b = 0; b < TK::L::kBoxes; ++b)
+        tma_store_3d(&tm_dk, sK + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) rv[k] = 0u;
-          }
-          uint32_t pv[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            pv[k] = pack2<kBf16>(dvs * __uint_as_float(rv[2 * k]), dvs * __uint_as_float(rv[2 * k + 1]));
-          *reinterpret_cast<uint4*>(sV + TV::offset(r, c0)) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
-          *reinterpret_cast<uint4*>(sV + TV::offset(r, c0 + 8)) = make_uint4(pv[4], pv[5], pv[6], pv[7]);
-        }
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t rk[16];
-          if (nsteps > 0) {
-            tmem_ld16(tmem + C::kColDK + lane_off + c0, rk);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) rk[k] = 0u;
-          }
-          uint32_t pkk[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            pkk[k] = pack2<kBf16>(p.c * __uint_as_float(rk[2 * k]), p.c * __uint_as_float(rk[2 * k + 1]));
-          *reinterpret_cast<uint4*>(sK + TK::offset(r, c0)) = make_uint4(pkk[0], pkk[1], pkk[2], pkk[3]);
-          *reinterpret_cast<uint4*>(sK + TK::offset(r, c0 + 8)) =
-              make_uint4(pkk[4], pkk[5], pkk[6], pkk[7]);
-        }
-      }
-      fence_proxy_async_smem();
-      named_barrier(2, 128);
-      if (ok && r == 0) {
-#pragma unroll
-        for (int b = 0; b < TK::L::kBoxes; ++b)
-          tma_store_3d(&tm_dk, sK + b * TK::kBoxBytes, b * TK::L::kBoxCols, key0, bh);
-#pragma unroll
-        for (int b = 0; b < TV::L::kBoxes; ++b)
-          tma_store_3d(&tm_dv, sV + b * TV::kBoxBytes, b * TV::L::kBoxCols, key0, bh);
-        tma_store_commit();
-        tma_store_wait_all();
-      }
+      for (int b = 0; b < TV::L::kBoxes; ++b)
+        tma_store_3d(&tm_dv, sV + b * TV::kBoxBytes, b * TV::L::kBoxCols, key0, bh);
+      tma_store_commit();
+      tma_store_wait_all();
     }
   }
 

@@ -575,39 +575,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ds_full);
     }
-    // ---------------------------------------------------------------- epilogue (warps 3-6)
-    // dQ = c * (dS K) rounded and stored through the (now idle) Q tile.
-    if (half == 0 && row0 < n) {
-      if (ok && nsteps > 0) ok = mbar_wait_spin(&bars.dq_done, 0, p.status, 49);
-      tc_fence_after();
-      if (ok) {
+    // ---------------------------------------------------------------- epilogue
+    // dQ = c * (dS K) rounded and stored through the (now idle) Q tile: each half of the warps
+    // stages half of the columns (half 0 all of them when a half would be narrower than 16).
+    constexpr int kSplit = D / 2 >= 16 ? 2 : 1;
+    constexpr int kWq = D / kSplit;
+    if (ok && nsteps > 0) ok = mbar_wait_spin(&bars.dq_done, 0, p.status, 49);
+    tc_fence_after();
+    if (ok && half < kSplit)
+      bwd::stage_acc<kBf16, TQ, kWq>(tmem + C::kColDQ + lane_off + half * kWq, p.c, sQ, r,
+                                     half * kWq, nsteps > 0);
+    fence_proxy_async_smem();
+    bwd::named_barrier(2, kSoftmaxWarps * 32);
+    if (ok && half == 0 && r == 0) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          uint32_t rr[16];
-          if (nsteps > 0) {
-            tmem_ld16(tmem + C::kColDQ + lane_off + c0, rr);
-            tmem_wait_ld();
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) rr[k] = 0u;
-          }
-          uint32_t pk[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            pk[k] = pack2<kBf16>(p.c * __uint_as_float(rr[2 * k]), p.c * __uint_as_float(rr[2 * k + 1]));
-          *reinterpret_cast<uint4*>(sQ + TQ::offset(r, c0)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(sQ + TQ::offset(r, c0 + 8)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-      fence_proxy_async_smem();
-      bwd::named_barrier(2, 128);
-      if (ok && r == 0) {
-#pragma unroll
-        for (int b = 0; b < TQ::L::kBoxes; ++b)
-          tma_store_3d(&tm_dq, sQ + b * TQ::kBoxBytes, b * TQ::L::kBoxCols, row0, bh);
-        tma_store_commit();
-        tma_store_wait_all();
-      }
+      for (int b = 0; b < TQ::L::kBoxes; ++b)
+        tma_store_3d(&tm_dq, sQ + b * TQ::kBoxBytes, b * TQ::L::kBoxCols, row0, bh);
+      tma_store_commit();
+      tma_store_wait_all();
     }
   }
 
