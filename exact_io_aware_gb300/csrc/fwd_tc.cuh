@@ -671,25 +671,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = l > 0.0f ? (kDrop ? p.drop.scale : 1.0f) / l : 0.0f;
       uint8_t* stage = sQ + t * C::kQSlot;  // Q_t is dead once every MMA of tile t is done
       if (ok) {
+        // up to 64 columns of O loaded before one wait
+        constexpr int kB = DV < 64 ? DV : 64;
 #pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 16) {
-          uint32_t rr[16];
+        for (int c0 = 0; c0 < DV; c0 += kB) {
+          uint32_t rr[kB];
           if (active) {
-            tmem_ld16(tO + lane_off + c0, rr);
+#pragma unroll
+            for (int c = 0; c < kB; c += 16)
+              tmem_ld16(tO + lane_off + c0 + c, *reinterpret_cast<uint32_t(*)[16]>(rr + c));
             tmem_wait_ld();
           } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) rr[k] = 0u;
+            for (int k = 0; k < kB; ++k) rr[k] = 0u;
           }
-          uint32_t pk[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            pk[k] = pack2<kBf16>(__uint_as_float(rr[2 * k]) * inv,
-                                 __uint_as_float(rr[2 * k + 1]) * inv);
-          *reinterpret_cast<uint4*>(stage + TO::offset(r, c0)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(stage + TO::offset(r, c0 + 8)) =
-              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          for (int c = 0; c < kB; c += 8) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              pk[k] = pack2<kBf16>(__uint_as_float(rr[c + 2 * k]) * inv,
+                                   __uint_as_float(rr[c + 2 * k + 1]) * inv);
+            *reinterpret_cast<uint4*>(stage + TO::offset(r, c0 + c)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
         if (row < nrow) {
           p.lse[static_cast<int64_t>(bh) * n + row] =
