@@ -21,12 +21,15 @@
 // Roles:
 //   warp  0    TMEM allocator and MMA issuer (lowest warp slot: the warp schedulers favour it
 //              over the softmax warps it shares a sub-partition with)
-//   warps 1-8  softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 1) / 4 of the
-//              block's query columns (P and dS are elementwise, so the halves never meet);
-//              warps 1-4 also write dK and dV at the end
-//   warp  9    TMA producer (K, V once; Q, dO, LSE, D per block through an NS-stage ring)
-// Issue order per block i: dV_i, S_{i+1}, dK_i, dP_{i+1}: S_{i+1} follows dV_i, the last reader
-// of P_i, and dP_{i+1} follows dK_i, the last reader of dS_i.
+//   warps 1-8  softmax: warp w owns TMEM lanes 32 (w % 4).. and, of the block's query
+//              columns, the 32-column chunks 64 t + 32 h (h = (w - 1) / 4; P and dS are
+//              elementwise, so the warps never meet); P is published in two halves (chunks
+//              t = 0, then t = 1); at the end warps 1-4 write dV and warps 5-8 dK
+//   warp  9    TMA producer (K, V once; dO, Q, LSE, D per block through an NS-stage ring, dO
+//              and Q on barriers of their own)
+// Issue order per block i: dV_i (its first four k-steps once P's first half is stored),
+// S_{i+1}, dK_i, dP_{i+1}: S_{i+1} follows dV_i, the last reader of P_i, and dP_{i+1} follows
+// dK_i, the last reader of dS_i.
 // Dropout (kDrop): the mask of dropout.cuh is redrawn for the block's (query, key) pairs; the
 // dV operand is P with dropped pairs zeroed (dV is scaled by 1/(1-p) in the epilogue), and
 // dS = P (keep ? dP/(1-p) : 0) - P D uses the unzeroed P.

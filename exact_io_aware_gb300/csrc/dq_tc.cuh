@@ -12,8 +12,9 @@
 // the columns) and writes the row table (LSE_i log2 e and D_i) that the dK/dV kernel, launched
 // after it, copies per query block.
 // Q and dO are the same for every key block, so the softmax warps write them into tensor
-// memory once (the rows they load for D_i anyway; 16-bit pairs per column, the A-operand
-// layout), and all three products read only their B operand from shared memory.  With both
+// memory once (the rows they read for D_i anyway, from the tile's Q, dO and O staged in
+// shared memory by TMA; 16-bit pairs per column, the A-operand layout), and all three
+// products read only their B operand from shared memory.  With both
 // operands in shared memory a 128 x 128 x 16 product needs the SM's whole shared-memory
 // bandwidth, and the products ran at ~88 instead of ~64 cycles.  Per key block j:
 //   S  = Q K_jᵀ           (A = Q in tensor memory; one buffer, free again as soon as the
@@ -30,10 +31,12 @@
 //   warp  1    TMA producer of the K ring (NSK stages); blocks a few steps ahead are
 //              requested into L2
 //   warp  2    TMA producer of the V ring (NSV stages): the two rings are released by
-//              different products (K after dQ, V after dP), so neither waits on the other
+//              different products (K after dQ, V after dP), so neither waits on the other;
+//              it first stages the tile's Q, dO and O (its last two stages hold dO and O
+//              until the softmax warps have read them)
 //   warps 3-10 softmax: warp w owns TMEM lanes 32 (w % 4).. and half (w - 3) / 4 of the
-//              block's key columns (and of Q's and dO's columns when it loads them); warps
-//              3-6 also write dQ at the end
+//              block's key columns (and of Q's and dO's columns when it stages them); each
+//              half writes half of dQ's columns at the end
 // Issue order per block i: [S_{i+1} once S_i is loaded], dQ_i once dS_i is written, then
 // dP_{i+1}, which overwrites dS_i after dQ_i has read it (one thread's MMAs run in issue
 // order).  The softmax warps compute P_{i+1} while dQ_i and dP_{i+1} run, and the tensor core
