@@ -228,8 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int n = p.n;
-  const int bh = blockIdx.y;
-  const int key0 = blockIdx.x * kKeys;
+  // heaviest (causal: the first) key tiles first, by groups of heads (work_item)
+  const uint32_t wgroup = p.mask_kind == kMaskCausal ? kCausalHeadGroup : 1u;
+  uint32_t wrank, whead;
+  work_item(blockIdx.y * gridDim.x + blockIdx.x, gridDim.x, gridDim.y, wgroup, wrank, whead);
+  const int bh = static_cast<int>(whead);
+  const int key0 = static_cast<int>(wrank) * kKeys;
   const int nqb = (n + BQ - 1) / BQ;
 
   // ---------------------------------------------------------------- prologue
@@ -339,8 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t nx = gridDim.x, ny = gridDim.y;
         const uint32_t later = blockIdx.y * nx + blockIdx.x + p.next_cta;
         if (later < nx * ny) {
-          const int key0_l = static_cast<int>(later % nx) * kKeys;
-          const int bh_l = static_cast<int>(later / nx);
+          uint32_t rank_l, head_l;
+          work_item(later, nx, ny, wgroup, rank_l, head_l);
+          const int key0_l = static_cast<int>(rank_l) * kKeys;
+          const int bh_l = static_cast<int>(head_l);
           const int q0_l = p.mask_kind == kMaskCausal ? key0_l : 0;
 #pragma unroll
           for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_k, b * TK::L::kBoxCols, key0_l, bh_l);

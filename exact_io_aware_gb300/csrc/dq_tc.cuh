@@ -161,8 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int n = p.n;
-  const int bh = blockIdx.y;
-  const int tile = gridDim.x - 1 - blockIdx.x;  // heaviest (causal) query tiles first
+  // heaviest (causal) query tiles first, by groups of heads (work_item)
+  const uint32_t wgroup = p.mask_kind == kMaskCausal ? kCausalHeadGroup : 1u;
+  uint32_t wrank, whead;
+  work_item(blockIdx.y * gridDim.x + blockIdx.x, gridDim.x, gridDim.y, wgroup, wrank, whead);
+  const int bh = static_cast<int>(whead);
+  const int tile = static_cast<int>(gridDim.x - 1 - wrank);
   const int row0 = tile * kRows;
   const int nblk = (n + BN - 1) / BN;
 
@@ -263,8 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t nx = gridDim.x, ny = gridDim.y;
       const uint32_t later = blockIdx.y * nx + blockIdx.x + p.next_cta;
       if (later < nx * ny) {
-        const int row0_l = (static_cast<int>(nx) - 1 - static_cast<int>(later % nx)) * kRows;
-        const int bh_l = static_cast<int>(later / nx);
+        uint32_t rank_l, head_l;
+        work_item(later, nx, ny, wgroup, rank_l, head_l);
+        const int row0_l = (static_cast<int>(nx) - 1 - static_cast<int>(rank_l)) * kRows;
+        const int bh_l = static_cast<int>(head_l);
 #pragma unroll
         for (int b = 0; b < TK::L::kBoxes; ++b) tma_prefetch_l2_3d(&tm_q, b * TK::L::kBoxCols, row0_l, bh_l);
 #pragma unroll

@@ -55,6 +55,24 @@ __device__ __forceinline__ auto ring_of(const Ring& r) {
     return StaticRing<N>{};
   }
 }
+
+// Work item of CTA c in launch order (c = blockIdx.y * nx + blockIdx.x) for a grid of nx items
+// per head (rank 0 the heaviest) over ny heads.  Heads are taken in groups of `group`, and
+// within a group the items of all its heads go heaviest first: under the causal mask the
+// launch then ends on the lightest items of the last group instead of on each head's
+// heaviest, which would otherwise start last and hold the tail.  group = 1 is head by head.
+__device__ __forceinline__ void work_item(uint32_t c, uint32_t nx, uint32_t ny, uint32_t group,
+                                          uint32_t& rank, uint32_t& head) {
+  const uint32_t per = group * nx;
+  const uint32_t g = c / per;
+  const uint32_t h0 = g * group;
+  const uint32_t gh = min(group, ny - h0);
+  const uint32_t r = c - g * per;
+  rank = r / gh;
+  head = h0 + r % gh;
+}
+// Heads per group of the causal work order (16 heads' K, V, Q and dO stay within L2).
+constexpr uint32_t kCausalHeadGroup = 16;
 #endif
 
 // Stage count of a ring at launch: the caller's cap (0 = none) within [lo, hi].
